@@ -1,0 +1,567 @@
+#!/usr/bin/env python3
+"""Throughput of the fused adaLN row kernels on one GB300 (or N replicas).
+
+Metric: fused norm+modulate achieved HBM GB/s and % of the GB300 roofline;
+rows/s.  A step is one pass of the FLUX.1-shaped LayerNorm + modulate site
+over one batch: x [1, 4608, 3072] and its CFG pair x [2, 4608, 3072] with
+per-batch scale/shift rows (two launches of ln_modulate).  Algorithmic bytes
+are the minimum traffic: read x, scale, shift once, write out once.
+
+Inputs are seeded synthetic tensors (workloads.py), resident in HBM, rotated
+over enough buffer sets that every timed step reads from DRAM, not L2.  The
+timed region is bracketed by a barrier and a device synchronise; kernels are
+timed with CUDA events on the stream they run on.  Besides the headline the
+JSON line carries: the roofline of the dominant kernel, the oracle timed on
+the host cores (cpu_baseline), an end-to-end number through the C ABI from
+pinned host buffers (e2e), sampled SM clocks, and a per-entry-point table on
+the other model-site shapes.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl rmsmod|reference]
+
+For N > 1 launch one process per GPU (torchrun); every rank runs its own
+replica of the step (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused norm+modulate achieved HBM GB/s and % of GB300 roofline; rows/s"
+WORKLOAD = "flux_ln_modulate_1x4608x3072+cfg_2x4608x3072"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------------------
+# small utilities
+# --------------------------------------------------------------------------
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.tmp = None
+        self.marks = []
+
+    def start(self):
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def mark(self, label):
+        self.marks.append((label, time.time()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        rows = []
+        try:
+            with open(self.tmp.name) as fh:
+                for line in fh:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.tmp.name)
+        except Exception:
+            pass
+        return rows
+
+    @staticmethod
+    def summarise(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for name, v in zip(names[1:], r[5:9]):
+                if v.strip().lower() in ("active", "0x1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------
+# the reference arm: the CPU oracle, as it stands
+# --------------------------------------------------------------------------
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    import workloads as W
+
+    oracle.build()
+    B1 = W.WORKLOADS["ln_modulate_flux_1x4608x3072"].make()
+    B2 = W.WORKLOADS["ln_modulate_flux_cfg_2x4608x3072"].make()
+    # bounded sample per step: 8 rows of the B=1 tensor and 8 rows of each
+    # CFG batch (16 rows), the same mix as the GPU step
+    r1, r2 = 8, 8
+    x1 = np.ascontiguousarray(B1["x"][:, :r1])
+    x2 = np.ascontiguousarray(B2["x"][:, :r2])
+    D = B1["D"]
+    rows = r1 + 2 * r2
+    step_bytes = rows * D * 4 + 2 * D * 2 + 2 * 2 * D * 2
+
+    def step():
+        oracle.ln_modulate(x1, B1["scale"], B1["shift"])
+        oracle.ln_modulate(x2, B2["scale"], B2["shift"])
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = step_bytes * args.steps / dt / 1e9
+    sample = (f"per step {rows} rows of D=3072 ({r1} of x[1,4608,3072], {r2} per CFG batch of "
+              f"x[2,4608,3072]), single-threaded C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "rows_per_step": rows},
+        "rows_per_s": rows * args.steps / dt,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------------------
+# the CUDA arm
+# --------------------------------------------------------------------------
+
+def traffic_record(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (the summary records the source digest)."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    src = os.path.join(ROOT, "rmsnorm_modulate_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(src)):
+        with open(os.path.join(src, f), "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()[:16]
+    try:
+        with open(path) as fh:
+            for line in fh:
+                cells = [c.strip() for c in line.strip().strip("|").split("|")]
+                if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload:
+                    if cells[2] == digest:
+                        return int(float(cells[3]))
+    except OSError:
+        pass
+    return None
+
+
+def cpu_baseline(seconds: float):
+    import numpy as np
+
+    import oracle
+    import workloads as W
+
+    oracle.build()
+    B1 = W.WORKLOADS["ln_modulate_flux_1x4608x3072"].make()
+    x = np.ascontiguousarray(B1["x"][:, :64])
+    D = B1["D"]
+    per = 64 * D * 4 + 2 * D * 2
+    n = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        oracle.ln_modulate(x, B1["scale"], B1["shift"])
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": per * n / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} calls x 64 rows of x[1,4608,3072] (D=3072) through the single-"
+                      f"threaded C oracle, {dt:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="rmsmod", choices=["rmsmod", "reference"])
+    ap.add_argument("--no-kernels", action="store_true", help="skip the per-entry-point table")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import numpy as np
+    import torch
+
+    import workloads as W
+    from rmsnorm_modulate_gb300 import _build
+
+    if rank == 0:
+        _build.build()
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+        if rank != 0:
+            _build.build()  # no-op once rank 0 has built
+        dist.barrier()
+    import rmsnorm_modulate_gb300 as rm
+
+    lib = rm.library()
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    peak, peak_kind = peaks()
+
+    # ---- inputs (identical bits to the test-suite's) --------------------
+    def to_dev(bits):
+        a = np.ascontiguousarray(bits)
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    w1 = W.WORKLOADS["ln_modulate_flux_1x4608x3072"].make()
+    w2 = W.WORKLOADS["ln_modulate_flux_cfg_2x4608x3072"].make()
+    D = w1["D"]
+    rows1, rows2 = w1["B"] * w1["S"], w2["B"] * w2["S"]
+    sc1, sh1 = to_dev(w1["scale"]), to_dev(w1["shift"])
+    sc2, sh2 = to_dev(w2["scale"]), to_dev(w2["shift"])
+    x1_0, x2_0 = to_dev(w1["x"]), to_dev(w2["x"])
+    set_bytes = (rows1 + rows2) * D * 2 * 2
+    nsets = max(2, -(-4 * l2 // set_bytes) + 1)
+    sets = []
+    for i in range(nsets):
+        x1 = x1_0 if i == 0 else x1_0.clone()
+        x2 = x2_0 if i == 0 else x2_0.clone()
+        sets.append((x1, x2, torch.empty_like(x1), torch.empty_like(x2)))
+    step_bytes = rows1 * D * 4 + 2 * D * 2 + rows2 * D * 4 + 2 * 2 * D * 2
+    step_rows = rows1 + rows2
+    # the two launches per step as ready-made C-ABI argument tuples
+    stream = torch.cuda.Stream(device=dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    P = ctypes.c_void_p
+    calls = []
+    for x1, x2, o1, o2 in sets:
+        calls.append(((P(x1.data_ptr()), P(sc1.data_ptr()), P(sh1.data_ptr()), P(o1.data_ptr()),
+                       1, rows1, D, 0, ctypes.c_float(1e-6), None, None, sp),
+                      (P(x2.data_ptr()), P(sc2.data_ptr()), P(sh2.data_ptr()), P(o2.data_ptr()),
+                       2, w2["S"], D, D, ctypes.c_float(1e-6), None, None, sp)))
+    f = lib.ln_modulate
+
+    def launch(i):
+        a, b = calls[i % nsets]
+        if f(*a) != 0 or f(*b) != 0:
+            raise RuntimeError("ln_modulate launch failed")
+
+    uuid = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{uuid}" if uuid is not None else str(local)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+
+    # ---- warm-up (plus a short untimed ramp so clocks settle) ------------
+    with torch.cuda.stream(stream):
+        t_ramp = time.time()
+        i = 0
+        while i < args.warmup or time.time() - t_ramp < 0.3:
+            launch(i)
+            i += 1
+            if i % 256 == 0:
+                stream.synchronize()
+        stream.synchronize()
+
+    # ---- timed region -----------------------------------------------------
+    n_ev = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_ev)]
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.mark("timed_start")
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            a, b = calls[i % nsets]
+            e = ev[i]
+            e[0].record(stream)
+            if f(*a) != 0:
+                raise RuntimeError("ln_modulate launch failed")
+            e[1].record(stream)
+            if f(*b) != 0:
+                raise RuntimeError("ln_modulate launch failed")
+            e[2].record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.mark("timed_end")
+    if pg is not None:
+        pg.barrier()
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    k1 = [e[0].elapsed_time(e[1]) for e in ev]
+    k2 = [e[1].elapsed_time(e[2]) for e in ev]
+    if pg is not None:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * step_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    # dominant kernel: ln_modulate (both launches are the same kernel at D=3072)
+    kern_ms = (sum(k1) + sum(k2)) / args.steps
+    achieved = step_bytes / (kern_ms * 1e-3) / 1e9
+    b1 = rows1 * D * 4 + 2 * D * 2
+    b2 = rows2 * D * 4 + 2 * 2 * D * 2
+    per_launch = {
+        "ln_modulate_1x4608x3072": {"us": 1e3 * sum(k1) / len(k1),
+                                    "gbs": b1 / (sum(k1) / len(k1) * 1e-3) / 1e9},
+        "ln_modulate_2x4608x3072": {"us": 1e3 * sum(k2) / len(k2),
+                                    "gbs": b2 / (sum(k2) / len(k2) * 1e-3) / 1e9},
+    }
+    traffic = traffic_record("row_kernel<0,12,1>", "ln_modulate_flux_2x4608x3072")
+
+    # ---- end to end through the C ABI from pinned host buffers -----------
+    e2e = None
+    if not args.no_e2e:
+        x1h = torch.empty(x1_0.shape, dtype=torch.bfloat16).pin_memory()
+        x2h = torch.empty(x2_0.shape, dtype=torch.bfloat16).pin_memory()
+        x1h.copy_(x1_0.cpu())
+        x2h.copy_(x2_0.cpu())
+        o1h = torch.empty_like(x1h).pin_memory()
+        o2h = torch.empty_like(x2h).pin_memory()
+        sc1h, sh1h = sc1.cpu().pin_memory(), sh1.cpu().pin_memory()
+        sc2h, sh2h = sc2.cpu().pin_memory(), sh2.cpu().pin_memory()
+        x1d, x2d, o1d, o2d = sets[0]
+        sc1d, sh1d, sc2d, sh2d = (torch.empty_like(t) for t in (sc1, sh1, sc2, sh2))
+        e_steps = max(3, min(args.steps, 200))
+
+        def e2e_step():
+            for d_, h_ in ((x1d, x1h), (x2d, x2h), (sc1d, sc1h), (sh1d, sh1h), (sc2d, sc2h),
+                           (sh2d, sh2h)):
+                d_.copy_(h_, non_blocking=True)
+            rm.ln_modulate(x1d, sc1d, sh1d, out=o1d, stream=stream)
+            rm.ln_modulate(x2d, sc2d, sh2d, out=o2d, stream=stream)
+            o1h.copy_(o1d, non_blocking=True)
+            o2h.copy_(o2d, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                e2e_step()
+            stream.synchronize()
+            if pg is not None:
+                pg.barrier()
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for _ in range(e_steps):
+                e2e_step()
+            s1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = s0.elapsed_time(s1)
+        if pg is not None:
+            t = torch.tensor([e_ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = (x1h.numel() + x2h.numel() + sc1h.numel() + sh1h.numel() + sc2h.numel() +
+               sh2h.numel()) * 2
+        d2h = (o1h.numel() + o2h.numel()) * 2
+        e2e = {"value": world * step_bytes * e_steps / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+               "ms_per_step": e_ms / e_steps}
+
+    # ---- the other entry points on their model-site shapes ---------------
+    kernels = None
+    if not args.no_kernels:
+        kernels = kernel_table(rm, lib, dev, stream, l2, peak)
+    clocks = ClockSampler.summarise(sampler.stop())
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "rows_per_step": step_rows, "D": D,
+                   "bytes_per_step": step_bytes,
+                   "l2": f"{nsets} rotating input/output sets, {nsets * set_bytes / 2**20:.0f} "
+                         f"MiB > 4x the {l2 / 2**20:.0f} MiB L2",
+                   "parallelism": f"replicas x{world}"},
+        "rows_per_s": world * step_rows * args.steps / (total_ms * 1e-3),
+        "pct_of_roofline": 100.0 * value / world / peak,
+        "pct_of_nominal_8tbs": 100.0 * value / world / NOMINAL_HBM_GBS,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "row_kernel<0,12,1> (ln_modulate, D=3072)",
+                     "peak_kind": f"{peak_kind} copy bandwidth (burst)",
+                     "algorithmic_bytes_per_launch": {"B1": b1, "B2": b2}},
+        "per_launch": per_launch,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu_baseline(args.cpu_seconds) if world == 1 else None,
+        "kernels": kernels,
+    }
+    print(json.dumps(line))
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def kernel_table(rm, lib, dev, stream, l2, peak, iters=200):
+    """Every fused entry point on its model-site shape: median launch time
+    over rotating buffers, achieved GB/s against the algorithmic bytes."""
+    import torch
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+
+    def normal(shape, std=1.0, mean=0.0, dtype=torch.bfloat16):
+        t = torch.randn(*shape, generator=g, device=dev, dtype=torch.float32)
+        return (t * std + mean).to(dtype)
+
+    rows = {}
+
+    def timed(name, bytes_, nrows, calls):
+        nsets = len(calls)
+        with torch.cuda.stream(stream):
+            for i in range(5):
+                calls[i % nsets]()
+            stream.synchronize()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(iters)]
+            for i in range(iters):
+                evs[i][0].record(stream)
+                calls[i % nsets]()
+                evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        ts = sorted(a.elapsed_time(b) for a, b in evs)
+        med = ts[len(ts) // 2]
+        gbs = bytes_ / (med * 1e-3) / 1e9
+        rows[name] = {"us": med * 1e3, "gbs": gbs, "frac": gbs / peak,
+                      "rows_per_s": nrows / (med * 1e-3), "bytes": bytes_, "sets": nsets}
+
+    def nsets_for(set_bytes):
+        """Enough rotating sets that each launch's buffers were evicted from L2."""
+        return 1 if set_bytes >= 4 * l2 else min(16, -(-4 * l2 // set_bytes) + 1)
+
+    # ln_modulate, the small config (L2-resident at any rotation: latency-bound)
+    x = normal((1, 256, 1024))
+    sc, sh = normal((1, 1, 1024), 0.1), normal((1, 1, 1024), 0.1)
+    outs = [torch.empty_like(x) for _ in range(8)]
+    timed("ln_modulate_1x256x1024", 256 * 1024 * 4 + 4 * 1024, 256,
+          [lambda o=o: rm.ln_modulate(x, sc, sh, out=o, stream=stream) for o in outs])
+
+    # RMSNorm + modulate, ERNIE-Image
+    S, D = 4216, 4096
+    n = nsets_for(S * D * 4)
+    xs = [normal((1, S, D)) for _ in range(n)]
+    w = normal((D,), 0.05, 1.0)
+    sc, sh = normal((1, 1, D), 0.1), normal((1, 1, D), 0.1)
+    os_ = [torch.empty_like(xs[0]) for _ in range(n)]
+    timed("rmsnorm_modulate_1x4216x4096", S * D * 4 + 3 * D * 2, S,
+          [lambda a=a, o=o: rm.rmsnorm_modulate(a, w, sc, sh, out=o, stream=stream)
+           for a, o in zip(xs, os_)])
+    del xs, os_
+    # gated, ERNIE-Image
+    n = nsets_for(S * D * 8)
+    rs_in = [normal((1, S, D)) for _ in range(n)]
+    us = [normal((1, S, D)) for _ in range(n)]
+    gate = normal((1, 1, D), 0.1)
+    rs = [torch.empty_like(rs_in[0]) for _ in range(n)]
+    os_ = [torch.empty_like(rs_in[0]) for _ in range(n)]
+    timed("gated_rmsnorm_modulate_1x4216x4096", S * D * 8 + 4 * D * 2, S,
+          [lambda a=a, u=u, r=r, o=o: rm.gated_rmsnorm_modulate(a, u, gate, w, sc, sh, res_out=r,
+                                                                out=o, stream=stream)
+           for a, u, r, o in zip(rs_in, us, rs, os_)])
+    del rs_in, us, rs, os_
+    # qk-LayerNorm, GLM-Image
+    R = 4352 * 32
+    n = nsets_for(2 * R * 128 * 4)
+    qs = [normal((R, 128), 2.0) for _ in range(n)]
+    ks = [normal((R, 128), 2.0) for _ in range(n)]
+    wq, bq = normal((128,), 0.05, 1.0), normal((128,), 0.02)
+    wk, bk = normal((128,), 0.05, 1.0), normal((128,), 0.02)
+    qo = [torch.empty_like(qs[0]) for _ in range(n)]
+    ko = [torch.empty_like(qs[0]) for _ in range(n)]
+    timed("qk_layernorm_1x4352x32x128", 2 * R * 128 * 4 + 4 * 128 * 2, 2 * R,
+          [lambda a=a, b=b, c=c, d=d: rm.qk_layernorm(a, b, wq, bq, wk, bk, q_out=c, k_out=d,
+                                                      stream=stream)
+           for a, b, c, d in zip(qs, ks, qo, ko)])
+    del qs, ks, qo, ko
+    # channels-last RMSNorm + SiLU, Wan VAE
+    import workloads as W
+
+    for C in (96, 192, 384):
+        npx = W.WAN_PIXELS
+        xw = normal((npx, C))
+        bias = normal((C,), 0.1, dtype=torch.float32)
+        gam = normal((C,), 0.05, 1.0)
+        ow = torch.empty_like(xw)
+        timed(f"rmsnorm_silu_cl_wan_c{C}", npx * C * 4 + C * 4 + C * 2, npx,
+              [lambda: rm.rmsnorm_silu_cl(xw, bias, gam, out=ow, stream=stream)])
+        del xw, ow
+    torch.cuda.synchronize(dev)
+    return rows
+
+
+if __name__ == "__main__":
+    sys.exit(main())

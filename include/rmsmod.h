@@ -1,0 +1,209 @@
+/*
+ * rmsmod.h -- C ABI of librmsmod.so: fused adaLN row normalisation + modulate
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * Each entry point fuses what an eager diffusion-transformer adaLN site runs
+ * as several bandwidth-bound kernels into one pass over HBM, and reproduces
+ * the eager chain's bf16 rounding after every elementwise op:
+ *   R(v) = round fp32 -> bf16, nearest-even;  f(h) = exact bf16 -> fp32.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are device pointers.  bf16 tensors are passed as raw 16-bit
+ *     patterns (any type the caller likes, e.g. torch.bfloat16 storage).
+ *   - Row-major, innermost dimension contiguous (unit stride).  A "row" is
+ *     the vector that is normalised (D, head_dim or C values).
+ *   - Every bf16 pointer must be 16-byte aligned; D, head_dim and C must be
+ *     multiples of 8 (one 16-byte vector = 8 bf16); batch strides are in
+ *     elements and must be multiples of 8.  fp32 pointers must be 16-byte
+ *     aligned too (per-channel fp32 bias) or 4-byte aligned (per-row outputs).
+ *   - Row statistics are fp32: the exact mean / biased variance / mean square
+ *     of the row, rounded once to fp32; rstd = 1 / sqrt(stat + eps) as
+ *     three correctly rounded fp32 operations.
+ *   - The caller owns every buffer.  The library allocates nothing, needs no
+ *     workspace and keeps no global state other than cached device
+ *     attributes.  Calls are asynchronous on `stream` (NULL = the legacy
+ *     default stream); nothing synchronises the host.
+ *   - Output buffers may alias their row input exactly (out == x,
+ *     res_out == residual); any other overlap is rejected when detected and
+ *     is otherwise undefined.
+ *   - Errors: arguments are validated before anything is launched; on any
+ *     failure the call returns a negative rmsmod_status and launches
+ *     nothing.  A zero row count returns RMSMOD_OK and launches nothing.
+ *     There is no fallback inside the library: a caller that wants one
+ *     tests rmsmod_supported() or the returned status and runs its own.
+ *
+ * Sources (web pages describing the method):
+ *   [GLM]   sglang PR #34008 "GLM-Image bit-exact fused aten LayerNorm+modulate / qk-LN"
+ *   [ERNIE] sglang PR #33854 "ERNIE-Image bit-exact fused RMSNorm+scale/shift"
+ *   [FLUX]  sglang PR #34004 "FLUX.1 fused adaLN modulate (bit-exact) + RoPE cache hoist"
+ *   [QWEN]  RL-Kernel PR #538 "[Qwen-Image][CUDA] Final AdaLN output (final_adaln_out)"
+ *   [WAN]   sglang PR #38650 "Fuse the Wan VAE conv bias epilogue and tile the RMSNorm+SiLU kernel"
+ */
+#ifndef RMSMOD_H
+#define RMSMOD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* rmsmod_stream_t;
+
+typedef enum {
+    RMSMOD_OK = 0,
+    RMSMOD_ERR_NULL = -1,        /* a required pointer is NULL */
+    RMSMOD_ERR_SHAPE = -2,       /* negative size, D/C/head_dim not a multiple of 8,
+                                    above the supported maximum, C == 1, ... */
+    RMSMOD_ERR_ALIGN = -3,       /* a pointer is not aligned as required */
+    RMSMOD_ERR_STRIDE = -4,      /* a batch stride is negative or not a multiple of 8 */
+    RMSMOD_ERR_UNSUPPORTED = -5, /* partially overlapping buffers or another unsupported combination */
+    RMSMOD_ERR_CUDA = -6,        /* the CUDA runtime reported an error at launch */
+    RMSMOD_ERR_DEVICE = -7       /* no usable CUDA device is current */
+} rmsmod_status;
+
+/* Largest supported row length D (ln / rms / gated) and channel count C. */
+#define RMSMOD_MAX_D 16384
+#define RMSMOD_MAX_C 1024
+
+/* ------------------------------------------------------------------------
+ * ln_modulate -- LayerNorm without affine, then the adaLN modulate chain.
+ *   [GLM] §Motivation (GlmImageAdaLayerNormZero) and §What "rounding-faithful"
+ *   means here; [QWEN] §What (out = LayerNorm(x, eps, no affine) * (1 + scale) + shift);
+ *   [FLUX] §Modifications commit 2 (per-op rounding of the modulate chain).
+ *
+ *   For each row r = (b, s) of x [B, S, D]:
+ *     mean, var  = fp32 mean and biased variance of f(x[r, :])
+ *     rstd       = 1 / sqrt(var + eps)
+ *     y[d]       = R((f(x[r,d]) - mean) * rstd)                (no FMA)
+ *     out[r, d]  = R(f(R(f(y[d]) * f(R(1 + f(scale_b[d]))))) + f(shift_b[d]))
+ *   scale_b = scale + b * mod_bstride (elements; 0 = one row for every batch),
+ *   same for shift_b: this covers per-batch CFG rows and adaLN chunk views.
+ *
+ *   x, out        bf16 [B*S*D], out may equal x
+ *   scale, shift  bf16, each row D values at base + b * mod_bstride
+ *   mean_out, rstd_out  nullable fp32 [B*S]
+ * ---------------------------------------------------------------------- */
+int ln_modulate(const void* x, const void* scale, const void* shift, void* out,
+                int64_t B, int64_t S, int64_t D, int64_t mod_bstride, float eps,
+                float* mean_out, float* rstd_out, rmsmod_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * rmsnorm_modulate -- RMSNorm (optional weight), then the modulate chain.
+ *   [ERNIE] §What "rounding-faithful" means here (rstd from sum_sq / H + eps;
+ *   one final rounding of x * rstd * w; the aten modulate chain).
+ *
+ *     ms    = fp32 mean of f(x)^2 over the row;  rstd = 1 / sqrt(ms + eps)
+ *     y[d]  = R((f(x[d]) * rstd) * f(w[d]))       (w = 1 when weight is NULL)
+ *     out   = modulate chain of ln_modulate.
+ *   weight nullable bf16 [D]; rstd_out nullable fp32 [B*S].
+ * ---------------------------------------------------------------------- */
+int rmsnorm_modulate(const void* x, const void* weight, const void* scale, const void* shift,
+                     void* out, int64_t B, int64_t S, int64_t D, int64_t mod_bstride,
+                     float eps, float* rstd_out, rmsmod_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * gated_rmsnorm_modulate -- gated residual add, then RMSNorm + modulate.
+ *   [ERNIE] §What "rounding-faithful" means here (residual variant) and
+ *   §Modifications (the second site returns the residual stream too).
+ *
+ *     res[r, d] = R(f(residual[r,d]) + f(R(f(gate_b[d]) * f(update[r,d]))))
+ *     out       = rmsnorm_modulate(res)  (statistics over res)
+ *   residual, update, res_out, out  bf16 [B*S*D]; res_out may equal residual.
+ *   gate bf16 rows at gate + b * gate_bstride; weight nullable bf16 [D].
+ * ---------------------------------------------------------------------- */
+int gated_rmsnorm_modulate(const void* residual, const void* update, const void* gate,
+                           int64_t gate_bstride, const void* weight, const void* scale,
+                           const void* shift, int64_t mod_bstride, void* res_out, void* out,
+                           int64_t B, int64_t S, int64_t D, float eps, float* rstd_out,
+                           rmsmod_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * qk_layernorm -- per-head LayerNorm with affine over head_dim values, q rows
+ * and k rows in one launch, each tensor with its own weight and bias.
+ *   [GLM] §Motivation (qk-norm nn.LayerNorm(128) on (1, S, 32, 128)) and
+ *   §What "rounding-faithful" means here (q and k in one launch).
+ *
+ *     z[d] = R(((f(x[d]) - mean) * rstd) * f(w[d]) + f(b[d]))
+ *   q, q_out [rows_q * head_dim]; k, k_out [rows_k * head_dim] (bf16);
+ *   wq, bq, wk, bk bf16 [head_dim]; head_dim must be 128.
+ *   mean_out, rstd_out nullable fp32 [rows_q + rows_k], q rows first.
+ * ---------------------------------------------------------------------- */
+int qk_layernorm(const void* q, const void* k, const void* wq, const void* bq, const void* wk,
+                 const void* bk, void* q_out, void* k_out, int64_t rows_q, int64_t rows_k,
+                 int64_t head_dim, float eps, float* mean_out, float* rstd_out,
+                 rmsmod_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * rmsnorm_silu_cl -- channels-last RMSNorm * gamma, then SiLU, with the
+ * deferred conv bias folded in first.
+ *   [WAN] §Quality-gated (tiled [ROWS, C] RMSNorm+SiLU, optional conv_bias)
+ *   and §New kernel, lossless (bias arithmetic of aten add_).
+ *
+ *   x is a dense channels-last activation viewed as `pixels` rows of C:
+ *     xb[c]  = R(f(x[c]) + f(b16[c]))   b16 = R(bias[c]) for an fp32 bias;
+ *                                       xb = x when bias is NULL
+ *     rstd   = 1 / sqrt(fp32 mean of f(xb)^2 + eps)
+ *     z[c]   = (f(xb[c]) * rstd) * f(gamma[c])        (fp32, unrounded)
+ *     out[c] = R(z / (1 + exp(-z)))
+ *   bias nullable ([C] fp32 when bias_is_fp32, else bf16); gamma bf16 [C];
+ *   C a multiple of 8 in [8, RMSMOD_MAX_C]; rstd_out nullable fp32 [pixels].
+ * ---------------------------------------------------------------------- */
+int rmsnorm_silu_cl(const void* x, const void* bias, int bias_is_fp32, const void* gamma,
+                    void* out, int64_t pixels, int64_t C, float eps, float* rstd_out,
+                    rmsmod_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Standalone elementwise chains (the fused kernels' epilogue / prologue,
+ * exported on their own; bit-exact to the eager chain by construction).
+ * ---------------------------------------------------------------------- */
+
+/* modulate_scale_shift: out = R(f(R(f(y) * f(R(1 + f(scale_b))))) + f(shift_b)) over
+ * y [B, S, D]; rows of scale/shift at base + b * mod_bstride.
+ *   [FLUX] §Modifications commit 2 (modulate_scale_shift: round(round(x * round(1+scale)) + shift)). */
+int modulate_scale_shift(const void* y, const void* scale, const void* shift, void* out,
+                         int64_t B, int64_t S, int64_t D, int64_t mod_bstride,
+                         rmsmod_stream_t stream);
+
+/* residual_gate_add: res = R(f(residual) + f(R(f(gate_b) * f(update)))) over [B, S, D].
+ *   [GLM] §Motivation (ff gate) and [ERNIE] §What (residual variant). */
+int residual_gate_add(const void* residual, const void* gate, const void* update,
+                      int64_t gate_bstride, void* res_out, int64_t B, int64_t S, int64_t D,
+                      rmsmod_stream_t stream);
+
+/* conv_bias_epilogue: out = R(f(x) + f(b16)); with a residual h (nullable):
+ * out = R(f(R(f(x) + f(b16))) + f(h)).  x, h, out: `pixels` channels-last rows of C.
+ *   [WAN] §New kernel, lossless. */
+int conv_bias_epilogue(const void* x, const void* bias, int bias_is_fp32, const void* h,
+                       void* out, int64_t pixels, int64_t C, rmsmod_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Predicates and diagnostics
+ * ---------------------------------------------------------------------- */
+
+enum {
+    RMSMOD_OP_LN_MODULATE = 1,
+    RMSMOD_OP_RMSNORM_MODULATE = 2,
+    RMSMOD_OP_GATED_RMSNORM_MODULATE = 3,
+    RMSMOD_OP_QK_LAYERNORM = 4,
+    RMSMOD_OP_RMSNORM_SILU_CL = 5
+};
+
+/* 1 if `op` supports row length / channel count `D_or_C` and every non-NULL
+ * pointer in ptrs[0..nptrs) is suitably aligned; 0 otherwise.  Never fails,
+ * never touches the GPU.  ([WAN] §New kernel: the predicate never raises;
+ * the kernel validates.) */
+int rmsmod_supported(int op, int64_t D_or_C, const void* const* ptrs, int nptrs);
+
+/* Static text for a status code (never NULL). */
+const char* rmsmod_status_string(int status);
+
+/* ABI version of this header: major * 10000 + minor * 100 + patch. */
+int rmsmod_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSMOD_H */

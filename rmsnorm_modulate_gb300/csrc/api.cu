@@ -1,0 +1,516 @@
+// C ABI of librmsmod.so: argument validation, device-attribute cache and
+// dispatch to the kernel translation units.  Every check runs on the host
+// before any CUDA call, so a rejected call touches neither the device nor
+// the CUDA runtime.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/rmsmod.h"
+#include "launch.h"
+
+#define RMSMOD_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+using rmsmod::DeviceInfo;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// [p, p + bytes) and [q, q + bytes2) overlap
+bool overlap(const void* p, int64_t bytes, const void* q, int64_t bytes2)
+{
+    if (!p || !q || bytes <= 0 || bytes2 <= 0)
+        return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(p), b0 = reinterpret_cast<uintptr_t>(q);
+    return a0 < b0 + static_cast<uintptr_t>(bytes2) && b0 < a0 + static_cast<uintptr_t>(bytes);
+}
+
+// An output may coincide exactly with its own input; any other overlap is an error.
+bool bad_alias(const void* out, const void* in, int64_t bytes, bool exact_ok)
+{
+    if (out == in)
+        return !exact_ok;
+    return overlap(out, bytes, in, bytes);
+}
+
+// rows * D as bytes, or -1 on overflow
+int64_t tensor_bytes(int64_t rows, int64_t D)
+{
+    if (rows < 0 || D < 0)
+        return -1;
+    if (D != 0 && rows > (INT64_MAX / 4) / D)
+        return -1;
+    return rows * D * 2;
+}
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[64];
+bool g_dev_valid[64];
+
+int device_info(DeviceInfo& info)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return RMSMOD_ERR_DEVICE;
+    }
+    if (dev < 0 || dev >= 64)
+        return RMSMOD_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!g_dev_valid[dev]) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms <= 0) {
+            cudaGetLastError();
+            return RMSMOD_ERR_DEVICE;
+        }
+        g_dev[dev] = DeviceInfo{dev, sms};
+        g_dev_valid[dev] = true;
+    }
+    info = g_dev[dev];
+    return RMSMOD_OK;
+}
+
+int launch_status(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return RMSMOD_OK;
+    return RMSMOD_ERR_CUDA;
+}
+
+// Shape checks shared by the [B, S, D] operations.
+int check_bsd(int64_t B, int64_t S, int64_t D)
+{
+    if (B < 0 || S < 0 || D <= 0)
+        return RMSMOD_ERR_SHAPE;
+    if (D % 8 != 0 || D > RMSMOD_MAX_D)
+        return RMSMOD_ERR_SHAPE;
+    if (B != 0 && S > INT64_MAX / B)
+        return RMSMOD_ERR_SHAPE;
+    if (tensor_bytes(B * S, D) < 0)
+        return RMSMOD_ERR_SHAPE;
+    return RMSMOD_OK;
+}
+
+int check_bstride(int64_t s)
+{
+    if (s < 0 || s % 8 != 0)
+        return RMSMOD_ERR_STRIDE;
+    return RMSMOD_OK;
+}
+
+}  // namespace
+
+RMSMOD_EXPORT int rmsmod_version(void) { return 10000; }
+
+RMSMOD_EXPORT const char* rmsmod_status_string(int status)
+{
+    switch (status) {
+    case RMSMOD_OK:
+        return "ok";
+    case RMSMOD_ERR_NULL:
+        return "a required pointer is NULL";
+    case RMSMOD_ERR_SHAPE:
+        return "unsupported or inconsistent size";
+    case RMSMOD_ERR_ALIGN:
+        return "a pointer is not aligned as required (16 bytes for tensors)";
+    case RMSMOD_ERR_STRIDE:
+        return "a batch stride is negative or not a multiple of 8 elements";
+    case RMSMOD_ERR_UNSUPPORTED:
+        return "overlapping buffers or an unsupported combination of arguments";
+    case RMSMOD_ERR_CUDA:
+        return "the CUDA runtime reported an error at launch";
+    case RMSMOD_ERR_DEVICE:
+        return "no usable CUDA device is current";
+    default:
+        return "unknown status";
+    }
+}
+
+RMSMOD_EXPORT int rmsmod_supported(int op, int64_t D_or_C, const void* const* ptrs, int nptrs)
+{
+    if (D_or_C <= 0 || D_or_C % 8 != 0)
+        return 0;
+    switch (op) {
+    case RMSMOD_OP_LN_MODULATE:
+    case RMSMOD_OP_RMSNORM_MODULATE:
+    case RMSMOD_OP_GATED_RMSNORM_MODULATE:
+        if (D_or_C > RMSMOD_MAX_D)
+            return 0;
+        break;
+    case RMSMOD_OP_QK_LAYERNORM:
+        if (D_or_C != 128)
+            return 0;
+        break;
+    case RMSMOD_OP_RMSNORM_SILU_CL:
+        if (D_or_C > RMSMOD_MAX_C || D_or_C < 8)
+            return 0;
+        break;
+    default:
+        return 0;
+    }
+    if (nptrs < 0 || (nptrs > 0 && !ptrs))
+        return 0;
+    for (int i = 0; i < nptrs; ++i)
+        if (ptrs[i] && !aligned(ptrs[i], 16))
+            return 0;
+    return 1;
+}
+
+RMSMOD_EXPORT int ln_modulate(const void* x, const void* scale, const void* shift, void* out,
+                              int64_t B, int64_t S, int64_t D, int64_t mod_bstride, float eps,
+                              float* mean_out, float* rstd_out, rmsmod_stream_t stream)
+{
+    int st = check_bsd(B, S, D);
+    if (st != RMSMOD_OK)
+        return st;
+    if ((st = check_bstride(mod_bstride)) != RMSMOD_OK)
+        return st;
+    const int64_t rows = B * S;
+    if (rows == 0)
+        return RMSMOD_OK;
+    if (!x || !scale || !shift || !out)
+        return RMSMOD_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(scale, 16) || !aligned(shift, 16) || !aligned(out, 16) ||
+        !aligned(mean_out, 4) || !aligned(rstd_out, 4))
+        return RMSMOD_ERR_ALIGN;
+    const int64_t bytes = tensor_bytes(rows, D);
+    if (bad_alias(out, x, bytes, true) || overlap(out, bytes, scale, 2 * D) ||
+        overlap(out, bytes, shift, 2 * D) || overlap(mean_out, 4 * rows, out, bytes) ||
+        overlap(rstd_out, 4 * rows, out, bytes) || overlap(mean_out, 4 * rows, rstd_out, 4 * rows))
+        return RMSMOD_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    if ((st = device_info(dev)) != RMSMOD_OK)
+        return st;
+    rmsmod::RowArgs a{};
+    a.x = x;
+    a.scale = scale;
+    a.shift = shift;
+    a.mod_bstride = mod_bstride / 8;
+    a.out = out;
+    a.mean_out = mean_out;
+    a.rstd_out = rstd_out;
+    a.rows = rows;
+    a.S = S;
+    a.Dv = static_cast<int>(D / 8);
+    a.n = static_cast<float>(D);
+    a.inv_n = 1.0f / static_cast<float>(D);
+    a.eps = eps;
+    return launch_status(rmsmod::launch_row_kernel(rmsmod::kOpLN, a, dev, stream));
+}
+
+RMSMOD_EXPORT int rmsnorm_modulate(const void* x, const void* weight, const void* scale,
+                                   const void* shift, void* out, int64_t B, int64_t S, int64_t D,
+                                   int64_t mod_bstride, float eps, float* rstd_out,
+                                   rmsmod_stream_t stream)
+{
+    int st = check_bsd(B, S, D);
+    if (st != RMSMOD_OK)
+        return st;
+    if ((st = check_bstride(mod_bstride)) != RMSMOD_OK)
+        return st;
+    const int64_t rows = B * S;
+    if (rows == 0)
+        return RMSMOD_OK;
+    if (!x || !scale || !shift || !out)
+        return RMSMOD_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(weight, 16) || !aligned(scale, 16) || !aligned(shift, 16) ||
+        !aligned(out, 16) || !aligned(rstd_out, 4))
+        return RMSMOD_ERR_ALIGN;
+    const int64_t bytes = tensor_bytes(rows, D);
+    if (bad_alias(out, x, bytes, true) || overlap(out, bytes, weight, 2 * D) ||
+        overlap(out, bytes, scale, 2 * D) || overlap(out, bytes, shift, 2 * D) ||
+        overlap(rstd_out, 4 * rows, out, bytes))
+        return RMSMOD_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    if ((st = device_info(dev)) != RMSMOD_OK)
+        return st;
+    rmsmod::RowArgs a{};
+    a.x = x;
+    a.weight = weight;
+    a.scale = scale;
+    a.shift = shift;
+    a.mod_bstride = mod_bstride / 8;
+    a.out = out;
+    a.rstd_out = rstd_out;
+    a.rows = rows;
+    a.S = S;
+    a.Dv = static_cast<int>(D / 8);
+    a.n = static_cast<float>(D);
+    a.inv_n = 1.0f / static_cast<float>(D);
+    a.eps = eps;
+    return launch_status(rmsmod::launch_row_kernel(rmsmod::kOpRMS, a, dev, stream));
+}
+
+RMSMOD_EXPORT int gated_rmsnorm_modulate(const void* residual, const void* update,
+                                         const void* gate, int64_t gate_bstride,
+                                         const void* weight, const void* scale,
+                                         const void* shift, int64_t mod_bstride, void* res_out,
+                                         void* out, int64_t B, int64_t S, int64_t D, float eps,
+                                         float* rstd_out, rmsmod_stream_t stream)
+{
+    int st = check_bsd(B, S, D);
+    if (st != RMSMOD_OK)
+        return st;
+    if ((st = check_bstride(mod_bstride)) != RMSMOD_OK ||
+        (st = check_bstride(gate_bstride)) != RMSMOD_OK)
+        return st;
+    const int64_t rows = B * S;
+    if (rows == 0)
+        return RMSMOD_OK;
+    if (!residual || !update || !gate || !scale || !shift || !res_out || !out)
+        return RMSMOD_ERR_NULL;
+    if (!aligned(residual, 16) || !aligned(update, 16) || !aligned(gate, 16) ||
+        !aligned(weight, 16) || !aligned(scale, 16) || !aligned(shift, 16) ||
+        !aligned(res_out, 16) || !aligned(out, 16) || !aligned(rstd_out, 4))
+        return RMSMOD_ERR_ALIGN;
+    const int64_t bytes = tensor_bytes(rows, D);
+    if (bad_alias(res_out, residual, bytes, true) || bad_alias(res_out, update, bytes, false) ||
+        bad_alias(out, residual, bytes, false) || bad_alias(out, update, bytes, false) ||
+        bad_alias(out, res_out, bytes, false) || overlap(out, bytes, gate, 2 * D) ||
+        overlap(res_out, bytes, gate, 2 * D) || overlap(out, bytes, weight, 2 * D) ||
+        overlap(out, bytes, scale, 2 * D) || overlap(out, bytes, shift, 2 * D) ||
+        overlap(rstd_out, 4 * rows, out, bytes) || overlap(rstd_out, 4 * rows, res_out, bytes))
+        return RMSMOD_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    if ((st = device_info(dev)) != RMSMOD_OK)
+        return st;
+    rmsmod::RowArgs a{};
+    a.residual = residual;
+    a.update = update;
+    a.gate = gate;
+    a.gate_bstride = gate_bstride / 8;
+    a.weight = weight;
+    a.scale = scale;
+    a.shift = shift;
+    a.mod_bstride = mod_bstride / 8;
+    a.res_out = res_out;
+    a.out = out;
+    a.rstd_out = rstd_out;
+    a.rows = rows;
+    a.S = S;
+    a.Dv = static_cast<int>(D / 8);
+    a.n = static_cast<float>(D);
+    a.inv_n = 1.0f / static_cast<float>(D);
+    a.eps = eps;
+    return launch_status(rmsmod::launch_row_kernel(rmsmod::kOpGated, a, dev, stream));
+}
+
+RMSMOD_EXPORT int qk_layernorm(const void* q, const void* k, const void* wq, const void* bq,
+                               const void* wk, const void* bk, void* q_out, void* k_out,
+                               int64_t rows_q, int64_t rows_k, int64_t head_dim, float eps,
+                               float* mean_out, float* rstd_out, rmsmod_stream_t stream)
+{
+    if (rows_q < 0 || rows_k < 0 || head_dim != 128)
+        return RMSMOD_ERR_SHAPE;
+    if (tensor_bytes(rows_q, head_dim) < 0 || tensor_bytes(rows_k, head_dim) < 0 ||
+        rows_q > INT64_MAX / 2 - rows_k)
+        return RMSMOD_ERR_SHAPE;
+    if (rows_q + rows_k == 0)
+        return RMSMOD_OK;
+    if ((rows_q > 0 && (!q || !wq || !bq || !q_out)) ||
+        (rows_k > 0 && (!k || !wk || !bk || !k_out)))
+        return RMSMOD_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(wq, 16) || !aligned(bq, 16) ||
+        !aligned(wk, 16) || !aligned(bk, 16) || !aligned(q_out, 16) || !aligned(k_out, 16) ||
+        !aligned(mean_out, 4) || !aligned(rstd_out, 4))
+        return RMSMOD_ERR_ALIGN;
+    const int64_t bq_bytes = tensor_bytes(rows_q, head_dim);
+    const int64_t bk_bytes = tensor_bytes(rows_k, head_dim);
+    const int64_t nst = 4 * (rows_q + rows_k);
+    if (bad_alias(q_out, q, bq_bytes, true) || bad_alias(k_out, k, bk_bytes, true) ||
+        overlap(q_out, bq_bytes, k, bk_bytes) || overlap(k_out, bk_bytes, q, bq_bytes) ||
+        overlap(q_out, bq_bytes, k_out, bk_bytes) || overlap(mean_out, nst, rstd_out, nst) ||
+        overlap(q_out, bq_bytes, mean_out, nst) || overlap(k_out, bk_bytes, mean_out, nst) ||
+        overlap(q_out, bq_bytes, rstd_out, nst) || overlap(k_out, bk_bytes, rstd_out, nst))
+        return RMSMOD_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    int st;
+    if ((st = device_info(dev)) != RMSMOD_OK)
+        return st;
+    rmsmod::QkArgs a{};
+    a.q = q;
+    a.k = k;
+    a.wq = wq;
+    a.bq = bq;
+    a.wk = wk;
+    a.bk = bk;
+    a.q_out = q_out;
+    a.k_out = k_out;
+    a.mean_out = mean_out;
+    a.rstd_out = rstd_out;
+    a.rows_q = rows_q;
+    a.rows_k = rows_k;
+    a.eps = eps;
+    return launch_status(rmsmod::launch_qk_kernel(a, dev, stream));
+}
+
+RMSMOD_EXPORT int rmsnorm_silu_cl(const void* x, const void* bias, int bias_is_fp32,
+                                  const void* gamma, void* out, int64_t pixels, int64_t C,
+                                  float eps, float* rstd_out, rmsmod_stream_t stream)
+{
+    if (pixels < 0 || C < 8 || C % 8 != 0 || C > RMSMOD_MAX_C)
+        return RMSMOD_ERR_SHAPE;
+    if (tensor_bytes(pixels, C) < 0)
+        return RMSMOD_ERR_SHAPE;
+    if (pixels == 0)
+        return RMSMOD_OK;
+    if (!x || !gamma || !out)
+        return RMSMOD_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(bias, 16) || !aligned(gamma, 16) || !aligned(out, 16) ||
+        !aligned(rstd_out, 4))
+        return RMSMOD_ERR_ALIGN;
+    const int64_t bytes = tensor_bytes(pixels, C);
+    const int64_t bias_bytes = bias_is_fp32 ? 4 * C : 2 * C;
+    if (bad_alias(out, x, bytes, true) || overlap(out, bytes, bias, bias_bytes) ||
+        overlap(out, bytes, gamma, 2 * C) || overlap(rstd_out, 4 * pixels, out, bytes))
+        return RMSMOD_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    int st;
+    if ((st = device_info(dev)) != RMSMOD_OK)
+        return st;
+    rmsmod::WanArgs a{};
+    a.x = x;
+    a.bias = bias;
+    a.bias_is_fp32 = bias_is_fp32 ? 1 : 0;
+    a.gamma = gamma;
+    a.out = out;
+    a.rstd_out = rstd_out;
+    a.pixels = pixels;
+    a.Cv = static_cast<int>(C / 8);
+    a.n = static_cast<float>(C);
+    a.inv_n = 1.0f / static_cast<float>(C);
+    a.eps = eps;
+    return launch_status(rmsmod::launch_wan_kernel(a, dev, stream));
+}
+
+// ---- standalone elementwise chains --------------------------------------
+
+namespace {
+
+// Elementwise kernels index 16-byte vectors with 32-bit integers.
+constexpr int64_t kMaxEwVectors = (int64_t{1} << 31) - 1;
+
+int check_ew_rows(int64_t rows, int64_t D)
+{
+    if (rows < 0 || D <= 0 || D % 8 != 0 || D > (int64_t{1} << 30))
+        return RMSMOD_ERR_SHAPE;
+    if (tensor_bytes(rows, D) < 0 || rows * (D / 8) > kMaxEwVectors)
+        return RMSMOD_ERR_SHAPE;
+    return RMSMOD_OK;
+}
+
+}  // namespace
+
+RMSMOD_EXPORT int modulate_scale_shift(const void* y, const void* scale, const void* shift,
+                                       void* out, int64_t B, int64_t S, int64_t D,
+                                       int64_t mod_bstride, rmsmod_stream_t stream)
+{
+    if (B < 0 || S < 0 || (B != 0 && S > INT64_MAX / B))
+        return RMSMOD_ERR_SHAPE;
+    int st = check_ew_rows(B * S, D);
+    if (st != RMSMOD_OK)
+        return st;
+    if (S > UINT32_MAX)
+        return RMSMOD_ERR_SHAPE;
+    if ((st = check_bstride(mod_bstride)) != RMSMOD_OK)
+        return st;
+    if (B * S == 0)
+        return RMSMOD_OK;
+    if (!y || !scale || !shift || !out)
+        return RMSMOD_ERR_NULL;
+    if (!aligned(y, 16) || !aligned(scale, 16) || !aligned(shift, 16) || !aligned(out, 16))
+        return RMSMOD_ERR_ALIGN;
+    const int64_t bytes = tensor_bytes(B * S, D);
+    if (bad_alias(out, y, bytes, true) || overlap(out, bytes, scale, 2 * D) ||
+        overlap(out, bytes, shift, 2 * D))
+        return RMSMOD_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    if ((st = device_info(dev)) != RMSMOD_OK)
+        return st;
+    rmsmod::EwArgs a{};
+    a.a = y;
+    a.b = scale;
+    a.c = shift;
+    a.out = out;
+    a.bstride = mod_bstride / 8;
+    a.rows = B * S;
+    a.S = S;
+    a.Dv = static_cast<int>(D / 8);
+    return launch_status(rmsmod::launch_elementwise(rmsmod::kEwModulate, a, dev, stream));
+}
+
+RMSMOD_EXPORT int residual_gate_add(const void* residual, const void* gate, const void* update,
+                                    int64_t gate_bstride, void* res_out, int64_t B, int64_t S,
+                                    int64_t D, rmsmod_stream_t stream)
+{
+    if (B < 0 || S < 0 || (B != 0 && S > INT64_MAX / B))
+        return RMSMOD_ERR_SHAPE;
+    int st = check_ew_rows(B * S, D);
+    if (st != RMSMOD_OK)
+        return st;
+    if (S > UINT32_MAX)
+        return RMSMOD_ERR_SHAPE;
+    if ((st = check_bstride(gate_bstride)) != RMSMOD_OK)
+        return st;
+    if (B * S == 0)
+        return RMSMOD_OK;
+    if (!residual || !gate || !update || !res_out)
+        return RMSMOD_ERR_NULL;
+    if (!aligned(residual, 16) || !aligned(gate, 16) || !aligned(update, 16) ||
+        !aligned(res_out, 16))
+        return RMSMOD_ERR_ALIGN;
+    const int64_t bytes = tensor_bytes(B * S, D);
+    if (bad_alias(res_out, residual, bytes, true) || bad_alias(res_out, update, bytes, true) ||
+        overlap(res_out, bytes, gate, 2 * D))
+        return RMSMOD_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    if ((st = device_info(dev)) != RMSMOD_OK)
+        return st;
+    rmsmod::EwArgs a{};
+    a.a = residual;
+    a.b = gate;
+    a.c = update;
+    a.out = res_out;
+    a.bstride = gate_bstride / 8;
+    a.rows = B * S;
+    a.S = S;
+    a.Dv = static_cast<int>(D / 8);
+    return launch_status(rmsmod::launch_elementwise(rmsmod::kEwGateAdd, a, dev, stream));
+}
+
+RMSMOD_EXPORT int conv_bias_epilogue(const void* x, const void* bias, int bias_is_fp32,
+                                     const void* h, void* out, int64_t pixels, int64_t C,
+                                     rmsmod_stream_t stream)
+{
+    int st = check_ew_rows(pixels, C);
+    if (st != RMSMOD_OK)
+        return st;
+    if (pixels == 0)
+        return RMSMOD_OK;
+    if (!x || !bias || !out)
+        return RMSMOD_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(bias, 16) || !aligned(h, 16) || !aligned(out, 16))
+        return RMSMOD_ERR_ALIGN;
+    const int64_t bytes = tensor_bytes(pixels, C);
+    const int64_t bias_bytes = bias_is_fp32 ? 4 * C : 2 * C;
+    if (bad_alias(out, x, bytes, true) || bad_alias(out, h, bytes, true) ||
+        overlap(out, bytes, bias, bias_bytes))
+        return RMSMOD_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    if ((st = device_info(dev)) != RMSMOD_OK)
+        return st;
+    rmsmod::EwArgs a{};
+    a.a = x;
+    a.b = bias;
+    a.c = h;
+    a.out = out;
+    a.bias_is_fp32 = bias_is_fp32 ? 1 : 0;
+    a.rows = pixels;
+    a.S = 1;
+    a.Dv = static_cast<int>(C / 8);
+    return launch_status(rmsmod::launch_elementwise(rmsmod::kEwBias, a, dev, stream));
+}

@@ -1,0 +1,118 @@
+// Host-side launch interface between the C ABI (api.cu) and the kernel
+// translation units.  Internal to librmsmod.so.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace rmsmod {
+
+struct DeviceInfo {
+    int device;
+    int sms;
+};
+
+// Integer division by a runtime constant: q = (umulhi(n, m) + n) >> s,
+// exact for every 32-bit n (Granlund-Montgomery round-up multiplier).
+struct FastDiv {
+    uint32_t d, m, s;
+
+    static FastDiv make(uint32_t d)
+    {
+        FastDiv f;
+        f.d = d;
+        uint32_t s = 0;
+        while ((1ull << s) < d)
+            ++s;
+        f.s = s;
+        f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << s) - d)) / d + 1);
+        return f;
+    }
+
+#ifdef __CUDACC__
+    __device__ __forceinline__ uint32_t div(uint32_t n) const
+    {
+        return static_cast<uint32_t>((static_cast<uint64_t>(__umulhi(n, m)) + n) >> s);
+    }
+#endif
+};
+
+enum RowOp : int { kOpLN = 0, kOpRMS = 1, kOpGated = 2 };
+
+struct RowArgs {
+    const void* x;         // LN / RMS input rows
+    const void* residual;  // gated
+    const void* update;
+    const void* gate;
+    int64_t gate_bstride;  // in 8-element vectors
+    const void* weight;    // nullable
+    const void* scale;
+    const void* shift;
+    int64_t mod_bstride;   // in 8-element vectors
+    void* res_out;
+    void* out;
+    float* mean_out;
+    float* rstd_out;
+    int64_t rows;
+    int64_t S;
+    int Dv;                // D / 8
+    float n;               // D
+    float inv_n;           // fp32(1 / D)
+    float eps;
+};
+
+cudaError_t launch_row_kernel(int op, const RowArgs& a, const DeviceInfo& dev,
+                              cudaStream_t stream);
+
+struct QkArgs {
+    const void* q;
+    const void* k;
+    const void* wq;
+    const void* bq;
+    const void* wk;
+    const void* bk;
+    void* q_out;
+    void* k_out;
+    float* mean_out;
+    float* rstd_out;
+    int64_t rows_q;
+    int64_t rows_k;
+    float eps;
+};
+
+cudaError_t launch_qk_kernel(const QkArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
+struct WanArgs {
+    const void* x;
+    const void* bias;  // nullable
+    int bias_is_fp32;
+    const void* gamma;
+    void* out;
+    float* rstd_out;
+    int64_t pixels;
+    int Cv;            // C / 8
+    float n;           // C
+    float inv_n;
+    float eps;
+};
+
+cudaError_t launch_wan_kernel(const WanArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
+enum EwOp : int { kEwModulate = 0, kEwGateAdd = 1, kEwBias = 2 };
+
+struct EwArgs {
+    const void* a;        // y / residual / x
+    const void* b;        // scale / gate / bias
+    const void* c;        // shift / update / h (nullable for bias)
+    void* out;
+    int64_t bstride;      // scale/shift or gate batch stride (vectors)
+    int bias_is_fp32;
+    int64_t rows;         // B*S or pixels
+    int64_t S;            // rows per batch (1 for the bias epilogue)
+    int Dv;               // row length in vectors
+};
+
+cudaError_t launch_elementwise(int op, const EwArgs& a, const DeviceInfo& dev,
+                               cudaStream_t stream);
+
+}  // namespace rmsmod

@@ -1,0 +1,242 @@
+// rmsnorm_silu_cl on sm_103a: channels-last RMSNorm * gamma + SiLU with the
+// deferred conv bias folded in (sglang #38650 Wan VAE, §Quality-gated and
+// §Modifications).
+//
+// In a channels_last(_3d) activation each pixel's C channels are contiguous
+// and consecutive pixels are adjacent, so a run of pixels is one contiguous
+// byte range.  P lanes share a pixel (V 16-byte vectors each, P * V * 8 >= C)
+// and a warp covers 32 / P consecutive pixels per step: every warp-wide load
+// instruction reads whole 32-byte sectors of one contiguous span.  A lane's
+// channels never change, so its bias (rounded to bf16 once) and gamma
+// (widened to fp32 once) stay in registers for the whole kernel.
+//
+//   xb  = R(x + R(bias))              (aten add_ arithmetic, before the statistics)
+//   z   = (xb * rstd) * gamma         (fp32, unrounded)
+//   out = R(z * sigmoid(z))
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace rmsmod {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+template <int N>
+struct Log2Ceil {
+    static constexpr int value = (N <= 1) ? 0 : 1 + Log2Ceil<(N + 1) / 2>::value;
+};
+template <>
+struct Log2Ceil<1> {
+    static constexpr int value = 0;
+};
+
+// SiLU(z) = z * sigmoid(z), sigmoid from e = exp(-|z|) in (0, 1] so nothing
+// overflows: sigmoid = 1 / (1 + e) for z >= 0 and e / (1 + e) below zero.
+__device__ __forceinline__ float silu(float z)
+{
+    const float e = expf(-fabsf(z));
+    const float r = __fdividef(1.0f, __fadd_rn(1.0f, e));
+    const float s = z >= 0.0f ? r : __fmul_rn(e, r);
+    return __fmul_rn(z, s);
+}
+
+template <int P, int V>
+__global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
+{
+    constexpr int kL = Log2Ceil<8 * V>::value;
+    constexpr int kPixPerWarp = 32 / P;
+    constexpr int kPixPerBlock = kPixPerWarp * (kThreads / 32);
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int sub = lane % P;
+    const int psub = lane / P;
+    const int Cv = a.Cv;
+
+    const uint4* __restrict__ x = static_cast<const uint4*>(a.x);
+    uint4* __restrict__ out = static_cast<uint4*>(a.out);
+    const bool has_bias = a.bias != nullptr;
+
+    // this lane's channels: vectors sub + P * j
+    uint32_t b16[V][4];
+    u64 g2[V][4];
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int c = sub + P * j;
+        uint4 g = make_uint4(0u, 0u, 0u, 0u), bb = make_uint4(0u, 0u, 0u, 0u);
+        if (c < Cv) {
+            g = ld_cached(static_cast<const uint4*>(a.gamma) + c);
+            if (has_bias) {
+                if (a.bias_is_fp32) {
+                    const float4* bf = static_cast<const float4*>(a.bias) + 2 * c;
+                    const float4 lo = ld_cached_f4(bf), hi = ld_cached_f4(bf + 1);
+                    bb = make_uint4(pack_bf2(lo.x, lo.y), pack_bf2(lo.z, lo.w),
+                                    pack_bf2(hi.x, hi.y), pack_bf2(hi.z, hi.w));
+                } else {
+                    bb = ld_cached(static_cast<const uint4*>(a.bias) + c);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            g2[j][i] = f2_from_bf2(word(g, i));
+            b16[j][i] = word(bb, i);
+        }
+    }
+
+    for (int64_t pix0 = (static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp) * kPixPerWarp;
+         pix0 < a.pixels; pix0 += static_cast<int64_t>(gridDim.x) * kPixPerBlock) {
+        const int64_t pix = pix0 + psub;
+        const bool valid = pix < a.pixels;
+        const int64_t base = pix * Cv;
+
+        uint4 xv[V];
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int c = sub + P * j;
+            if (valid && c < Cv) {
+                uint4 v = ld_stream(x + base + c);
+                if (has_bias) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        word(v, i) = bf2_add(word(v, i), b16[j][i]);
+                }
+                xv[j] = v;
+            } else {
+                xv[j] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+
+        uint32_t m = 0;
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                m = bf2_absmax(m, word(xv[j], i));
+        const uint32_t mm = absmax_bits(m);
+        const uint32_t E = offset_exponent(mm);
+
+        ExactSums<false> acc;
+        acc.init(offset_k1<kL>(E), offset_k2<kL>(E));
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                acc.add(f2_from_bf2(word(xv[j], i)));
+        float s1h, s1l, s2h, s2l;
+        acc.lane_total(s1h, s1l, s2h, s2l);
+        dd_allreduce<P>(s2h, s2l);
+        uint32_t cls = allreduce_max<P>(static_cast<uint32_t>(magnitude_class(mm)));
+        uint32_t emax = allreduce_max<P>(mm == 0 ? 0u : (mm >> 7));
+        float stat = finalize_ms(s2h, s2l, a.n, a.inv_n);
+
+        if (__any_sync(kFullMask, cls != kClassFast)) {
+            // Rare (Inf/NaN or extreme magnitudes in some pixel of this warp):
+            // every lane runs both slow variants; each pixel keeps its own.
+            float p2 = 0.0f;
+            RowScale rs;
+            rs.set(emax);
+            ExactSums<false> acc2;
+            acc2.init(offset_k1<kL>(127u), offset_k2<kL>(127u));
+#pragma unroll
+            for (int j = 0; j < V; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const u64 xx = f2_from_bf2(word(xv[j], i));
+                    float lo, hi;
+                    f2_unpack(xx, lo, hi);
+                    p2 = __fadd_rn(__fadd_rn(p2, __fmul_rn(lo, lo)), __fmul_rn(hi, hi));
+                    acc2.add(rs.apply(xx));
+                }
+            p2 = allreduce_add<P>(p2);
+            float t1h, t1l, t2h, t2l;
+            acc2.lane_total(t1h, t1l, t2h, t2l);
+            dd_allreduce<P>(t2h, t2l);
+            if (cls == kClassNonFinite)
+                stat = __fmul_rn(p2, a.inv_n);
+            else if (cls == kClassScaled)
+                stat = rs.unscale(finalize_ms(t2h, t2l, a.n, a.inv_n), 2);
+        }
+        const float rstd = rstd_from(stat, a.eps);
+        if (valid && sub == 0 && a.rstd_out)
+            a.rstd_out[pix] = rstd;
+
+        const u64 rstd2 = f2_splat(rstd);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int c = sub + P * j;
+            if (valid && c < Cv) {
+                uint4 o;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const u64 z = f2_mul(f2_mul(f2_from_bf2(word(xv[j], i)), rstd2), g2[j][i]);
+                    float z0, z1;
+                    f2_unpack(z, z0, z1);
+                    word(o, i) = pack_bf2(silu(z0), silu(z1));
+                }
+                st_stream(out + base + c, o);
+            }
+        }
+    }
+}
+
+template <int P, int V>
+cudaError_t launch_cfg(const WanArgs& a, const DeviceInfo& dev, cudaStream_t stream)
+{
+    auto kern = wan_kernel<P, V>;
+    static int blocks_per_sm[64] = {0};
+    const int d = dev.device & 63;
+    if (blocks_per_sm[d] == 0) {
+        int nb = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads, 0);
+        if (e != cudaSuccess)
+            return e;
+        blocks_per_sm[d] = nb > 0 ? nb : 1;
+    }
+    constexpr int kPixPerBlock = (32 / P) * (kThreads / 32);
+    const int64_t want = (a.pixels + kPixPerBlock - 1) / kPixPerBlock;
+    const int64_t cap = static_cast<int64_t>(dev.sms) * blocks_per_sm[d];
+    const int grid = static_cast<int>(want < cap ? want : cap);
+    kern<<<grid, kThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int P>
+cudaError_t launch_p(const WanArgs& a, const DeviceInfo& dev, cudaStream_t stream)
+{
+    const int V = (a.Cv + P - 1) / P;
+    switch (V) {
+    case 1:
+        return launch_cfg<P, 1>(a, dev, stream);
+    case 2:
+        return launch_cfg<P, 2>(a, dev, stream);
+    case 3:
+        return launch_cfg<P, 3>(a, dev, stream);
+    default:
+        return launch_cfg<P, 4>(a, dev, stream);
+    }
+}
+
+}  // namespace
+
+// P = the smallest power of two with P * 4 >= C / 8 (at most 32), so a lane
+// holds at most four vectors: C = 96 -> 4 lanes x 3, C = 192 -> 8 x 3,
+// C = 384 -> 16 x 3, C = 1024 -> 32 x 4.
+cudaError_t launch_wan_kernel(const WanArgs& a, const DeviceInfo& dev, cudaStream_t stream)
+{
+    const int need = (a.Cv + 3) / 4;
+    if (need <= 1)
+        return launch_p<1>(a, dev, stream);
+    if (need <= 2)
+        return launch_p<2>(a, dev, stream);
+    if (need <= 4)
+        return launch_p<4>(a, dev, stream);
+    if (need <= 8)
+        return launch_p<8>(a, dev, stream);
+    if (need <= 16)
+        return launch_p<16>(a, dev, stream);
+    return launch_p<32>(a, dev, stream);
+}
+
+}  // namespace rmsmod

@@ -1,0 +1,203 @@
+"""The C ABI without a GPU: the library loads, exports every entry point the
+public header declares, and rejects bad arguments on the host (status codes,
+nothing launched).  No call here passes a complete set of valid arguments,
+so nothing can reach a kernel launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rmsmod.h")
+
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_STRIDE, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE = \
+    0, -1, -2, -3, -4, -5, -6, -7
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rmsnorm_modulate_gb300 import _build
+
+    _build.build()
+    import rmsnorm_modulate_gb300 as rm
+
+    return rm.library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:int|char\s*\*|const char\s*\*)\s*\*?\s*"
+                                 r"([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = header_functions()
+    for n in ("ln_modulate", "rmsnorm_modulate", "gated_rmsnorm_modulate", "qk_layernorm",
+              "rmsnorm_silu_cl", "modulate_scale_shift", "residual_gate_add",
+              "conv_bias_epilogue", "rmsmod_supported", "rmsmod_status_string",
+              "rmsmod_version"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), f"librmsmod.so does not export {name}"
+
+
+def test_exports_are_plain_c_symbols(lib):
+    out = os.popen(f"nm -D --defined-only {lib._name}").read()
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    for name in header_functions():
+        assert name in exported
+    # nothing C++-mangled leaks into the dynamic symbol table
+    assert not [s for s in exported if s.startswith("_Z")]
+
+
+def test_status_strings(lib):
+    for st in (OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_STRIDE, ERR_UNSUPPORTED, ERR_CUDA,
+               ERR_DEVICE, 12345):
+        s = lib.rmsmod_status_string(st)
+        assert isinstance(s, bytes) and s
+    assert lib.rmsmod_version() == 10000
+
+
+P = ctypes.c_void_p
+A = 0x100000  # 16-byte aligned fake addresses, never dereferenced on the host
+MIS = 0x100008
+
+
+def p(v):
+    return P(v)
+
+
+def test_ln_modulate_validation(lib):
+    f = lib.ln_modulate
+    s = P(0)
+    # sizes
+    assert f(p(A), p(A + 4096), p(A + 8192), p(A + 1 << 24), 1, 4, 12, 0, 1e-6, None, None, s) \
+        == ERR_SHAPE                                       # D % 8
+    assert f(p(A), p(A), p(A), p(A), 1, 4, 0, 0, 1e-6, None, None, s) == ERR_SHAPE
+    assert f(p(A), p(A), p(A), p(A), -1, 4, 8, 0, 1e-6, None, None, s) == ERR_SHAPE
+    assert f(p(A), p(A), p(A), p(A), 1, 4, 16392, 0, 1e-6, None, None, s) == ERR_SHAPE
+    assert f(p(A), p(A), p(A), p(A), 1 << 40, 1 << 40, 8, 0, 1e-6, None, None, s) == ERR_SHAPE
+    # strides
+    assert f(p(A), p(A), p(A), p(A), 2, 4, 8, 4, 1e-6, None, None, s) == ERR_STRIDE
+    assert f(p(A), p(A), p(A), p(A), 2, 4, 8, -8, 1e-6, None, None, s) == ERR_STRIDE
+    # zero rows: OK, nothing launched even with NULL pointers
+    assert f(None, None, None, None, 0, 4, 8, 0, 1e-6, None, None, s) == OK
+    assert f(None, None, None, None, 3, 0, 8, 0, 1e-6, None, None, s) == OK
+    # NULLs
+    assert f(None, p(A), p(A), p(A), 1, 4, 8, 0, 1e-6, None, None, s) == ERR_NULL
+    assert f(p(A), None, p(A), p(A), 1, 4, 8, 0, 1e-6, None, None, s) == ERR_NULL
+    assert f(p(A), p(A), p(A), None, 1, 4, 8, 0, 1e-6, None, None, s) == ERR_NULL
+    # alignment
+    assert f(p(MIS), p(A), p(A), p(A), 1, 4, 8, 0, 1e-6, None, None, s) == ERR_ALIGN
+    assert f(p(A), p(A), p(MIS), p(A), 1, 4, 8, 0, 1e-6, None, None, s) == ERR_ALIGN
+    assert f(p(A), p(A), p(A), p(A), 1, 4, 8, 0, 1e-6, p(A + 2), None, s) == ERR_ALIGN
+    # partial overlap of out and x (exact aliasing is allowed)
+    assert f(p(A), p(A + 1 << 20), p(A + 1 << 21), p(A + 16), 1, 4, 8, 0, 1e-6, None, None, s) \
+        == ERR_UNSUPPORTED
+    # out overlapping scale
+    assert f(p(A), p(A + 4096 + 16), p(A + 1 << 21), p(A + 4096), 1, 4, 8, 0, 1e-6, None, None,
+             s) == ERR_UNSUPPORTED
+
+
+def test_rms_and_gated_validation(lib):
+    s = P(0)
+    r = lib.rmsnorm_modulate
+    assert r(p(A), p(MIS), p(A), p(A), p(A), 1, 2, 8, 0, 1e-6, None, s) == ERR_ALIGN
+    assert r(p(A), None, None, p(A), p(A), 1, 2, 8, 0, 1e-6, None, s) == ERR_NULL
+    assert r(p(A), None, p(A), p(A), p(A), 1, 2, 7, 0, 1e-6, None, s) == ERR_SHAPE
+    g = lib.gated_rmsnorm_modulate
+    args = [p(A), p(A + 1 << 20), p(A + 1 << 21), 0, None, p(A + 1 << 22), p(A + 1 << 23), 0,
+            p(A + 1 << 24), p(A + 1 << 25), 1, 2, 8, 1e-6, None, s]
+    bad = list(args)
+    bad[3] = 3
+    assert g(*bad) == ERR_STRIDE
+    bad = list(args)
+    bad[2] = None
+    assert g(*bad) == ERR_NULL
+    bad = list(args)
+    bad[9] = bad[0]  # out aliasing residual is not allowed (only res_out may)
+    assert g(*bad) == ERR_UNSUPPORTED
+    bad = list(args)
+    bad[9] = bad[8]  # out == res_out
+    assert g(*bad) == ERR_UNSUPPORTED
+
+
+def test_qk_validation(lib):
+    s = P(0)
+    f = lib.qk_layernorm
+    base = [p(A), p(A + 1 << 20), p(A + 1 << 21), p(A + 1 << 22), p(A + 1 << 23), p(A + 1 << 24),
+            p(A + 1 << 25), p(A + 1 << 26), 4, 4, 128, 1e-5, None, None, s]
+    bad = list(base)
+    bad[10] = 64
+    assert f(*bad) == ERR_SHAPE
+    bad = list(base)
+    bad[8] = -1
+    assert f(*bad) == ERR_SHAPE
+    bad = list(base)
+    bad[2] = None
+    assert f(*bad) == ERR_NULL
+    bad = list(base)
+    bad[6] = p(A + 16)  # q_out partially overlapping q
+    assert f(*bad) == ERR_UNSUPPORTED
+    bad = list(base)
+    bad[8], bad[9] = 0, 0
+    assert f(*bad) == OK
+
+
+def test_wan_and_elementwise_validation(lib):
+    s = P(0)
+    w = lib.rmsnorm_silu_cl
+    assert w(p(A), None, 1, p(A + 1 << 20), p(A + 1 << 21), 10, 4, 1e-6, None, s) == ERR_SHAPE
+    assert w(p(A), None, 1, p(A + 1 << 20), p(A + 1 << 21), 10, 1032, 1e-6, None, s) == ERR_SHAPE
+    assert w(p(A), p(A + 8), 1, p(A + 1 << 20), p(A + 1 << 21), 10, 96, 1e-6, None, s) == ERR_ALIGN
+    assert w(p(A), None, 1, None, p(A + 1 << 21), 10, 96, 1e-6, None, s) == ERR_NULL
+    assert w(None, None, 1, None, None, 0, 96, 1e-6, None, s) == OK
+    m = lib.modulate_scale_shift
+    assert m(p(A), p(A), p(A), p(A), 1, 2, 10, 0, s) == ERR_SHAPE
+    assert m(p(A), p(A), p(A), p(A), 2, 2, 8, 12, s) == ERR_STRIDE
+    assert m(p(A), None, p(A), p(A), 2, 2, 8, 0, s) == ERR_NULL
+    ga = lib.residual_gate_add
+    assert ga(p(A), p(A), p(MIS), 0, p(A), 1, 2, 8, s) == ERR_ALIGN
+    cb = lib.conv_bias_epilogue
+    assert cb(p(A), None, 1, None, p(A), 4, 96, s) == ERR_NULL
+    assert cb(p(A), p(A + 1 << 20), 1, p(MIS), p(A + 1 << 21), 4, 96, s) == ERR_ALIGN
+
+
+def test_supported_predicate(lib):
+    arr = (P * 3)(A, A + 32, None)
+    assert lib.rmsmod_supported(1, 3072, arr, 3) == 1
+    assert lib.rmsmod_supported(1, 3073, arr, 3) == 0
+    assert lib.rmsmod_supported(1, 16392, arr, 3) == 0
+    assert lib.rmsmod_supported(4, 128, arr, 3) == 1
+    assert lib.rmsmod_supported(4, 64, arr, 3) == 0
+    assert lib.rmsmod_supported(5, 96, arr, 3) == 1
+    assert lib.rmsmod_supported(5, 2048, arr, 3) == 0
+    assert lib.rmsmod_supported(99, 96, arr, 3) == 0
+    mis = (P * 2)(A, MIS)
+    assert lib.rmsmod_supported(2, 4096, mis, 2) == 0
+    assert lib.rmsmod_supported(2, 4096, None, 0) == 1
+    assert lib.rmsmod_supported(2, 4096, None, 2) == 0
+
+
+def test_valid_call_without_gpu_reports_device_error(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: a valid call would launch")
+    st = lib.ln_modulate(p(A), p(A + 1 << 20), p(A + 1 << 21), p(A + 1 << 22), 1, 4, 8, 0,
+                         1e-6, None, None, P(0))
+    assert st == ERR_DEVICE
+
+
+def test_binding_has_no_cpu_fallback():
+    torch = pytest.importorskip("torch")
+    import rmsnorm_modulate_gb300 as rm
+
+    x = torch.zeros(1, 4, 8, dtype=torch.bfloat16)
+    s = torch.zeros(8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        rm.ln_modulate(x, s, s)

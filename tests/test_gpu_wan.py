@@ -1,0 +1,93 @@
+"""Parity of rmsnorm_silu_cl (CUDA, through the C ABI) with the oracle.
+
+SiLU goes through the exponential: the GPU's fp32 exp and reciprocal differ
+from the oracle's double SiLU by a few fp32 ulps, which moves a bf16 rounding
+on a small fraction of elements -- within the 1-ulp bar, never beyond."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from _gpu import dev, host, stat_report
+from _util import assert_within_ulp
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rm():
+    import rmsnorm_modulate_gb300 as rm
+
+    return rm
+
+
+def run_wan(rm, oracle_mod, inp, eps=1e-6, max_ulp=1):
+    pixels, C = inp["pixels"], inp["C"]
+    rstd = torch.empty(pixels, dtype=torch.float32, device="cuda")
+    bias = None if inp["bias"] is None else dev(inp["bias"])
+    out = rm.rmsnorm_silu_cl(dev(inp["x"]), bias, dev(inp["gamma"]), eps, rstd_out=rstd)
+    torch.cuda.synchronize()
+    o_out, o_rstd = oracle_mod.rmsnorm_silu_cl(inp["x"], inp["bias"], inp["gamma"], eps)
+    assert stat_report(host(rstd), o_rstd)[1] <= 1e-5
+    d = assert_within_ulp(host(out), o_out, max_ulp=max_ulp)
+    return d, host(rstd), o_rstd
+
+
+@pytest.mark.parametrize("C", [8, 16, 32, 64, 96, 136, 192, 384, 512, 1024])
+@pytest.mark.parametrize("bias", ["fp32", "bf16", None])
+def test_channels(rm, oracle_mod, C, bias):
+    inp = W.wan_inputs(1000 + C, C, seed=C, bias_fp32=(bias != "bf16"))
+    if bias is None:
+        inp["bias"] = None
+    d, g, o = run_wan(rm, oracle_mod, inp)
+    assert np.array_equal(g, o)
+
+
+@pytest.mark.parametrize("C", [96, 192, 384])
+def test_wan_full_size_sampled(rm, oracle_mod, C):
+    """The full [1, C, 4, 480, 832] activation on the GPU; the oracle checks a
+    sample of 20000 pixel rows spread over the whole tensor."""
+    inp = W.WORKLOADS[f"rmsnorm_silu_cl_wan_c{C}"].make()
+    pixels = inp["pixels"]
+    x = dev(inp["x"])
+    rstd = torch.empty(pixels, dtype=torch.float32, device="cuda")
+    out = rm.rmsnorm_silu_cl(x, dev(inp["bias"]), dev(inp["gamma"]), 1e-6, rstd_out=rstd)
+    torch.cuda.synchronize()
+    idx = np.unique(np.concatenate([np.random.default_rng(C).integers(0, pixels, 20000),
+                                    [0, pixels - 1]]))
+    o_out, o_rstd = oracle_mod.rmsnorm_silu_cl(np.ascontiguousarray(inp["x"][idx]), inp["bias"],
+                                               inp["gamma"], 1e-6)
+    got = host(out[torch.from_numpy(idx).cuda()])
+    assert_within_ulp(got, o_out, max_ulp=1)
+    assert np.array_equal(host(rstd)[idx], o_rstd)
+
+
+def test_channels_last_5d_view(rm, oracle_mod):
+    C = 96
+    inp = W.wan_inputs(2 * 3 * 5, C, seed=3)
+    # a [1, C, 2, 3, 5] tensor in channels_last_3d memory format
+    x5 = dev(inp["x"]).view(1, 2, 3, 5, C).permute(0, 4, 1, 2, 3)
+    assert x5.is_contiguous(memory_format=torch.channels_last_3d)
+    out = rm.rmsnorm_silu_cl(x5, dev(inp["bias"]), dev(inp["gamma"]))
+    torch.cuda.synchronize()
+    o_out, _ = oracle_mod.rmsnorm_silu_cl(inp["x"], inp["bias"], inp["gamma"])
+    got = host(out.permute(0, 2, 3, 4, 1).reshape(-1, C))
+    assert_within_ulp(got, o_out, max_ulp=1)
+
+
+def test_bias_fold_identity(rm):
+    inp = W.wan_inputs(5000, 192, seed=11)
+    x, b, g = dev(inp["x"]), dev(inp["bias"]), dev(inp["gamma"])
+    a = rm.rmsnorm_silu_cl(x, b, g)
+    pre = rm.conv_bias_epilogue(x, b)
+    c = rm.rmsnorm_silu_cl(pre, None, g)
+    assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+
+
+def test_edge_and_special_rows(rm, oracle_mod):
+    for C in (96, 384):
+        for rows, labels in (W.edge_rows(C), W.special_rows(C)):
+            inp = W.wan_inputs(len(labels), C, seed=4)
+            inp["x"] = rows
+            inp["pixels"] = len(labels)
+            run_wan(rm, oracle_mod, inp, max_ulp=1)

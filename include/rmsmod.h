@@ -196,6 +196,15 @@ enum {
  * the kernel validates.) */
 int rmsmod_supported(int op, int64_t D_or_C, const void* const* ptrs, int nptrs);
 
+/* Device error word of the kernels launched so far on the current device:
+ * bit 0 (RMSMOD_DEVICE_ERR_COPY_TIMEOUT) = an asynchronous bulk copy into
+ * shared memory did not complete within the kernel's wait limit (1 s); the
+ * kernel then finished without that data instead of hanging, so its output
+ * is invalid.  Synchronous (it reads device memory); `clear` != 0 resets the
+ * word.  Returns RMSMOD_OK or RMSMOD_ERR_CUDA / RMSMOD_ERR_NULL. */
+#define RMSMOD_DEVICE_ERR_COPY_TIMEOUT 1u
+int rmsmod_device_status(unsigned int* bits, int clear);
+
 /* Static text for a status code (never NULL). */
 const char* rmsmod_status_string(int status);
 

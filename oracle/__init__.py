@@ -53,8 +53,14 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(_LIB)
+            # A test may point this at a deliberately mutated build of the
+            # oracle (tests/test_oracle_mutations.py); normally unset.
+            override = os.environ.get("RMSMOD_ORACLE_LIB")
+            if override:
+                lib = ctypes.CDLL(override)
+            else:
+                build()
+                lib = ctypes.CDLL(_LIB)
             P = ctypes.c_void_p
             I = ctypes.c_int64
             F = ctypes.c_float

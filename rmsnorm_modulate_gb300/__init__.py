@@ -23,7 +23,7 @@ import torch
 __all__ = [
     "RmsmodError", "library", "library_path", "ln_modulate", "rmsnorm_modulate",
     "gated_rmsnorm_modulate", "qk_layernorm", "rmsnorm_silu_cl", "modulate_scale_shift",
-    "residual_gate_add", "conv_bias_epilogue", "supported", "status_string",
+    "residual_gate_add", "conv_bias_epilogue", "supported", "status_string", "device_status",
     "OP_LN_MODULATE", "OP_RMSNORM_MODULATE", "OP_GATED_RMSNORM_MODULATE",
     "OP_QK_LAYERNORM", "OP_RMSNORM_SILU_CL",
 ]
@@ -77,6 +77,7 @@ def library() -> ctypes.CDLL:
             "rmsmod_supported": [C, I, ctypes.POINTER(P), C],
             "rmsmod_status_string": [C],
             "rmsmod_version": [],
+            "rmsmod_device_status": [ctypes.POINTER(ctypes.c_uint), C],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -328,6 +329,14 @@ def conv_bias_epilogue(x, bias, h=None, out=None, stream=None):
     _call("conv_bias_epilogue", _ptr(x), _ptr(bias), is32, _ptr(h), _ptr(out), pixels, C,
           _stream(stream))
     return out
+
+
+def device_status(clear: bool = False) -> int:
+    """Error bits recorded by kernels on the current device (0 = none).
+    Synchronous.  Bit 0: an asynchronous copy timed out (output invalid)."""
+    bits = ctypes.c_uint(0)
+    _call("rmsmod_device_status", ctypes.byref(bits), 1 if clear else 0)
+    return int(bits.value)
 
 
 def supported(op: int, d_or_c: int, *tensors) -> bool:

@@ -130,6 +130,21 @@ RMSMOD_EXPORT const char* rmsmod_status_string(int status)
     }
 }
 
+RMSMOD_EXPORT int rmsmod_device_status(unsigned int* bits, int clear)
+{
+    if (!bits)
+        return RMSMOD_ERR_NULL;
+    unsigned a = 0, b = 0, c = 0;
+    if (rmsmod::row_kernels_error(&a, clear != 0) != cudaSuccess ||
+        rmsmod::qk_kernel_error(&b, clear != 0) != cudaSuccess ||
+        rmsmod::wan_kernel_error(&c, clear != 0) != cudaSuccess) {
+        cudaGetLastError();
+        return RMSMOD_ERR_CUDA;
+    }
+    *bits = a | b | c;
+    return RMSMOD_OK;
+}
+
 RMSMOD_EXPORT int rmsmod_supported(int op, int64_t D_or_C, const void* const* ptrs, int nptrs)
 {
     if (D_or_C <= 0 || D_or_C % 8 != 0)

@@ -78,6 +78,102 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int i)
 }
 
 // ---------------------------------------------------------------------------
+// Asynchronous bulk copies (TMA, 1-D) into shared memory, tracked by mbarriers
+// ---------------------------------------------------------------------------
+
+// Longest a kernel waits for one bulk copy before it gives up, records an
+// error in its error word and carries on without the data (1 s).
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+// Error-word bits.
+constexpr unsigned kErrCopyTimeout = 1u;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Makes barrier initialisation visible to the asynchronous (TMA) proxy.
+__device__ __forceinline__ void mbar_init_fence()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses to shared memory before
+// later asynchronous-proxy writes (reuse of a buffer that was just read).
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// global -> shared bulk copy of `bytes` (multiple of 16, both addresses
+// 16-byte aligned); completion is signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase of `bar` with the given parity; false if it did not
+// complete within `limit_ns`.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit_ns)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (global_ns() - t0 > limit_ns)
+            return false;
+    }
+}
+
+// After a copy timed out: a bounded pause (1 ms) so that copies still in
+// flight land before the CTA exits and its shared memory is reused.
+__device__ __forceinline__ void drain_pause()
+{
+    const unsigned long long t0 = global_ns();
+    while (global_ns() - t0 < 1000000ull) {
+    }
+}
+
+// ---------------------------------------------------------------------------
 // bf16x2 (two bf16 in one 32-bit word: element 2i in the low half)
 // ---------------------------------------------------------------------------
 
@@ -180,6 +276,19 @@ __device__ __forceinline__ u64 f2_fma(u64 a, u64 b, u64 c)
 }
 
 __device__ __forceinline__ u64 f2_neg(u64 a) { return a ^ 0x8000000080000000ull; }
+
+// a * b then + c as two separately rounded fp32 operations.  The packed
+// f32x2 forms are not used here: a packed multiply feeding a packed add was
+// observed to come out fused, while __fmul_rn / __fadd_rn are documented
+// never to be merged into a multiply-add.
+__device__ __forceinline__ u64 f2_mul_then_add(u64 a, u64 b, u64 c)
+{
+    float a0, a1, b0, b1, c0, c1;
+    f2_unpack(a, a0, a1);
+    f2_unpack(b, b0, b1);
+    f2_unpack(c, c0, c1);
+    return f2_pack(__fadd_rn(__fmul_rn(a0, b0), c0), __fadd_rn(__fmul_rn(a1, b1), c1));
+}
 
 // ---------------------------------------------------------------------------
 // Double-float helpers (value = hi + lo, two fp32)

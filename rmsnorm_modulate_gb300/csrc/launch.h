@@ -115,4 +115,11 @@ struct EwArgs {
 cudaError_t launch_elementwise(int op, const EwArgs& a, const DeviceInfo& dev,
                                cudaStream_t stream);
 
+// Each kernel translation unit keeps a device error word (bit kErrCopyTimeout:
+// an asynchronous copy did not complete in time).  Reads it, optionally
+// clearing it; synchronous.
+cudaError_t row_kernels_error(unsigned* bits, bool clear);
+cudaError_t qk_kernel_error(unsigned* bits, bool clear);
+cudaError_t wan_kernel_error(unsigned* bits, bool clear);
+
 }  // namespace rmsmod

@@ -3,13 +3,14 @@
 // §What "rounding-faithful" means here, qk bullet).
 //
 // A 128-element head row is 256 bytes.  Four lanes own one row (32 values
-// each, as four 16-byte vectors), so one warp covers eight rows per step and
-// every lane is busy -- the eager kernel spends a 128-thread block per row
-// with three of its four warps idle.  A warp-instruction's 32 loads cover
-// eight 64-byte segments: full 32-byte sectors, no wasted DRAM bytes.
-// Blocks are split between the q rows and the k rows in proportion, so a
-// lane's weight and bias (32 columns, kept as fp32 pairs in registers) are
-// loaded once per kernel.
+// each, as four 16-byte vectors), so one warp covers a tile of eight
+// consecutive rows (2 KB) per step and every lane is busy -- the eager
+// kernel spends a 128-thread block per row with three of its four warps
+// idle.  Tiles reach shared memory by 1-D bulk copies (TMA) into a
+// four-stage ring per warp, so three tiles are in flight while one is
+// computed.  Blocks are split between the q rows and the k rows in
+// proportion, so a lane's weight and bias (32 columns, kept as fp32 pairs
+// in registers) are loaded once per kernel.
 //
 //   z = R(((x - mean) * rstd) * w + b)   -- fp32, one final rounding
 #include "device_common.cuh"
@@ -19,15 +20,23 @@ namespace rmsmod {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kLanesPerRow = 4;
-constexpr int kVecPerLane = 4;         // 4 x 8 = 32 values per lane
-constexpr int kRowsPerWarp = 32 / kLanesPerRow;
-constexpr int kRowsPerBlock = kRowsPerWarp * (kThreads / 32);
-constexpr int kL = 5;                  // 32 values per lane = 2^5
+__device__ unsigned int g_error;
 
-__global__ void __launch_bounds__(kThreads) qk_kernel(const QkArgs a, int blocks_q)
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kLanesPerRow = 4;
+constexpr int kVecPerLane = 4;                    // 4 x 8 = 32 values per lane
+constexpr int kTileRows = 32 / kLanesPerRow;      // rows per warp step
+constexpr int kTileVec = kTileRows * 16;          // 16-byte vectors per tile
+constexpr int kStages = 4;
+constexpr int kSmem = kWarps * kStages * kTileVec * 16;
+constexpr int kL = 5;                             // 32 values per lane = 2^5
+
+__global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blocks_q)
 {
+    extern __shared__ __align__(128) uint4 ring[];
+    __shared__ __align__(8) unsigned long long bars[kWarps][kStages];
+
     const bool is_q = static_cast<int>(blockIdx.x) < blocks_q;
     const int64_t rows = is_q ? a.rows_q : a.rows_k;
     const int blk = is_q ? blockIdx.x : blockIdx.x - blocks_q;
@@ -41,7 +50,7 @@ __global__ void __launch_bounds__(kThreads) qk_kernel(const QkArgs a, int blocks
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int sub = lane & (kLanesPerRow - 1);   // position inside the row
-    const int rsub = lane / kLanesPerRow;        // row inside the warp's eight
+    const int rsub = lane / kLanesPerRow;        // row inside the tile
 
     // this lane's columns: vectors sub, sub + 4, sub + 8, sub + 12
     u64 w2[kVecPerLane][4], b2[kVecPerLane][4];
@@ -56,18 +65,56 @@ __global__ void __launch_bounds__(kThreads) qk_kernel(const QkArgs a, int blocks
         }
     }
 
+    uint4* wbuf = ring + warp * kStages * kTileVec;
+    const uint32_t bar0 = smem_addr(&bars[warp][0]);
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < kStages; ++s)
+            mbar_init(bar0 + 8u * s, 1u);
+        mbar_init_fence();
+    }
+    __syncwarp();
+
+    const int64_t first = static_cast<int64_t>(blk) * kWarps + warp;  // tile index
+    const int64_t step = static_cast<int64_t>(nblk) * kWarps;
+    auto issue = [&](int64_t k) {
+        const int64_t row0 = (first + k * step) * kTileRows;
+        if (lane != 0 || row0 >= rows)
+            return;
+        const int64_t left = rows - row0;
+        const uint32_t bytes = static_cast<uint32_t>(left < kTileRows ? left : kTileRows) * 256u;
+        const int st = static_cast<int>(k % kStages);
+        const uint32_t bar = bar0 + 8u * st;
+        fence_proxy_async();
+        mbar_expect_tx(bar, bytes);
+        bulk_g2s(smem_addr(wbuf + st * kTileVec), src + row0 * 16, bytes, bar);
+    };
+#pragma unroll
+    for (int k = 0; k < kStages; ++k)
+        issue(k);
+
     const float n = 128.0f, inv_n = 1.0f / 128.0f;
-    for (int64_t row0 = (static_cast<int64_t>(blk) * (kThreads / 32) + warp) * kRowsPerWarp;
-         row0 < rows; row0 += static_cast<int64_t>(nblk) * kRowsPerBlock) {
+    bool broken = false;
+    for (int64_t k = 0; (first + k * step) * kTileRows < rows; ++k) {
+        const int64_t row0 = (first + k * step) * kTileRows;
+        const int st = static_cast<int>(k % kStages);
+        if (!broken && !mbar_wait(bar0 + 8u * st, static_cast<uint32_t>((k / kStages) & 1),
+                                  kWaitLimitNs)) {
+            broken = true;
+            if (lane == 0)
+                atomicOr(&g_error, kErrCopyTimeout);
+        }
         const int64_t row = row0 + rsub;
         const bool valid = row < rows;
         const int64_t base = row * 16;
 
+        const uint4* tile = wbuf + st * kTileVec + rsub * 16;
         uint4 xv[kVecPerLane];
 #pragma unroll
         for (int j = 0; j < kVecPerLane; ++j)
-            xv[j] = valid ? ld_stream(src + base + sub + kLanesPerRow * j)
-                          : make_uint4(0u, 0u, 0u, 0u);
+            xv[j] = valid ? tile[sub + kLanesPerRow * j] : make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+        issue(k + kStages);
 
         uint32_t m = 0;
 #pragma unroll
@@ -90,15 +137,13 @@ __global__ void __launch_bounds__(kThreads) qk_kernel(const QkArgs a, int blocks
         dd2_allreduce<kLanesPerRow>(s1h, s1l, s2h, s2l);
 
         // row class over its four lanes
-        uint32_t cls = static_cast<uint32_t>(magnitude_class(mm));
-        uint32_t emax = mm == 0 ? 0u : (mm >> 7);
-        cls = allreduce_max<kLanesPerRow>(cls);
-        emax = allreduce_max<kLanesPerRow>(emax);
+        uint32_t cls = allreduce_max<kLanesPerRow>(static_cast<uint32_t>(magnitude_class(mm)));
+        uint32_t emax = allreduce_max<kLanesPerRow>(mm == 0 ? 0u : (mm >> 7));
 
         float mean, var;
         finalize_ln(s1h, s1l, s2h, s2l, n, inv_n, mean, var);
         if (__any_sync(kFullMask, cls != kClassFast)) {
-            // Rare: some row of this warp holds Inf/NaN or extreme magnitudes.
+            // Rare: some row of this tile holds Inf/NaN or extreme magnitudes.
             // Every lane runs both slow variants (warp-uniform control flow)
             // and each row keeps the one its class asks for.
             float p1 = 0.0f, p2 = 0.0f;
@@ -147,14 +192,16 @@ __global__ void __launch_bounds__(kThreads) qk_kernel(const QkArgs a, int blocks
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const u64 xx = f2_from_bf2(word(xv[j], i));
-                    u64 z = f2_mul(f2_sub(xx, mean2), rstd2);
-                    z = f2_add(f2_mul(z, w2[j][i]), b2[j][i]);
+                    const u64 z = f2_mul_then_add(f2_mul(f2_sub(xx, mean2), rstd2), w2[j][i],
+                                                  b2[j][i]);
                     word(o, i) = bf2_from_f2(z);
                 }
                 st_stream(dst + base + sub + kLanesPerRow * j, o);
             }
         }
     }
+    if (broken)
+        drain_pause();
 }
 
 }  // namespace
@@ -164,12 +211,17 @@ cudaError_t launch_qk_kernel(const QkArgs& a, const DeviceInfo& dev, cudaStream_
     static int blocks_per_sm[64] = {0};
     const int d = dev.device & 63;
     if (blocks_per_sm[d] == 0) {
+        cudaError_t e =
+            cudaFuncSetAttribute(qk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e != cudaSuccess)
+            return e;
         int nb = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, qk_kernel, kThreads, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, qk_kernel, kThreads, kSmem);
         if (e != cudaSuccess)
             return e;
         blocks_per_sm[d] = nb > 0 ? nb : 1;
     }
+    constexpr int kRowsPerBlock = kTileRows * kWarps;
     const int64_t total = a.rows_q + a.rows_k;
     const int64_t cap = static_cast<int64_t>(dev.sms) * blocks_per_sm[d];
     const int64_t need_q = (a.rows_q + kRowsPerBlock - 1) / kRowsPerBlock;
@@ -187,8 +239,18 @@ cudaError_t launch_qk_kernel(const QkArgs& a, const DeviceInfo& dev, cudaStream_
         bk = cap - bq;
     }
     const int grid = static_cast<int>(bq + bk);
-    qk_kernel<<<grid, kThreads, 0, stream>>>(a, static_cast<int>(bq));
+    qk_kernel<<<grid, kThreads, kSmem, stream>>>(a, static_cast<int>(bq));
     return cudaGetLastError();
+}
+
+cudaError_t qk_kernel_error(unsigned* bits, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(bits, g_error, sizeof(unsigned));
+    if (e == cudaSuccess && clear && *bits) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_error, &zero, sizeof(unsigned));
+    }
+    return e;
 }
 
 }  // namespace rmsmod

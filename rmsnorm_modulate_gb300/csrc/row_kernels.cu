@@ -1,12 +1,16 @@
 // ln_modulate / rmsnorm_modulate / gated_rmsnorm_modulate on sm_103a.
 //
-// One warp (or a group of 2 / 4 warps for D > 4096) owns one row at a time
-// and loops persistently over rows.  The row is loaded once with 16-byte
-// streaming loads and stays in registers as packed bf16 while the exact
-// statistics are formed; the normalise + modulate epilogue then runs on
+// One warp (or a group of 2 / 4 warps for D > 4096, each owning a
+// contiguous segment of the row) processes one row at a time and loops
+// persistently over rows.  Rows arrive in shared memory by 1-D bulk copies
+// (TMA, cp.async.bulk) into a two-stage ring per warp, tracked by mbarriers:
+// while a warp computes row k, row k + 1 is already in flight, so HBM sees
+// a continuous stream independent of how long the arithmetic takes.  From
+// shared memory the row goes to registers as packed bf16, the exact
+// statistics are formed, and the normalise + modulate epilogue runs on
 // packed f32x2 / bf16x2 instructions and streams the result out.  HBM is
-// touched exactly once per element in each direction; scale, shift, weight
-// and gate rows are re-read from L1/L2.
+// touched once per element in each direction; scale, shift, weight and gate
+// rows are re-read from L1/L2.
 //
 // Arithmetic per element follows the eager chain of the pages:
 //   LayerNorm (sglang #34008 GLM-Image, §What "rounding-faithful" means here):
@@ -24,8 +28,8 @@ namespace rmsmod {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+// This translation unit's error word (see kErr* in device_common.cuh).
+__device__ unsigned int g_error;
 
 template <int N>
 struct Log2Ceil {
@@ -100,14 +104,37 @@ __device__ __forceinline__ void group_sum_plain(Slot* slots, int wig, int lane, 
     group_barrier<WPR>(group);
 }
 
+// Compile-time shape of one kernel instance.
 template <int OP, int V, int WPR>
-__global__ void __launch_bounds__(kThreads) row_kernel(const RowArgs a)
+struct RowShape {
+    static constexpr int kStages = 2;
+    static constexpr int kNbuf = (OP == kOpGated) ? 2 : 1;   // residual + update
+    static constexpr int kSegVec = 32 * V;                   // 16-byte vectors per buffer
+    static constexpr int kWarpBytes = kStages * kNbuf * kSegVec * 16;
+    // as many warps as ~96 KB of ring allows (two CTAs per SM), at most 8,
+    // a multiple of WPR
+    static constexpr int kFit = (96 * 1024) / kWarpBytes;
+    static constexpr int kWarps0 = kFit > 8 ? 8 : (kFit < 1 ? 1 : kFit);
+    static constexpr int kWarps = (kWarps0 / WPR) * WPR < WPR ? WPR : (kWarps0 / WPR) * WPR;
+    static constexpr int kThreads = 32 * kWarps;
+    static constexpr int kSmem = kWarps * kWarpBytes;
+};
+
+template <int OP, int V, int WPR>
+__global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads)
+    row_kernel(const RowArgs a)
 {
+    using Shape = RowShape<OP, V, WPR>;
+    constexpr int kWarps = Shape::kWarps;
     constexpr int kGroups = kWarps / WPR;
+    constexpr int kStages = Shape::kStages;
+    constexpr int kNbuf = Shape::kNbuf;
+    constexpr int kSegVec = Shape::kSegVec;
     constexpr int kL = Log2Ceil<8 * V>::value;
     constexpr bool kNeedSum = (OP == kOpLN);
-    // [parity][group][warp in group] for the common path, plus one slot row
-    // per group for the rare slow path.
+
+    extern __shared__ __align__(128) uint4 ring[];
+    __shared__ __align__(8) unsigned long long bars[kWarps][kStages];
     __shared__ Slot slots[2][kGroups][WPR];
     __shared__ Slot slow_slots[kGroups][WPR];
 
@@ -116,10 +143,16 @@ __global__ void __launch_bounds__(kThreads) row_kernel(const RowArgs a)
     const int group = warp / WPR;
     const int wig = warp % WPR;
     const int Dv = a.Dv;
+    // this warp's contiguous segment of every row
+    const int seg = (Dv + WPR - 1) / WPR;
+    const int s0 = wig * seg;
+    int seg_len = Dv - s0;
+    seg_len = seg_len > seg ? seg : (seg_len < 0 ? 0 : seg_len);
+    const uint32_t seg_bytes = static_cast<uint32_t>(seg_len) * 16u;
 
-    const uint4* __restrict__ x = static_cast<const uint4*>(a.x);
-    const uint4* __restrict__ residual = static_cast<const uint4*>(a.residual);
-    const uint4* __restrict__ update = static_cast<const uint4*>(a.update);
+    const uint4* __restrict__ src0 =
+        static_cast<const uint4*>(OP == kOpGated ? a.residual : a.x);
+    const uint4* __restrict__ src1 = static_cast<const uint4*>(a.update);
     const uint4* __restrict__ gate = static_cast<const uint4*>(a.gate);
     const uint4* __restrict__ weight = static_cast<const uint4*>(a.weight);
     const uint4* __restrict__ scale = static_cast<const uint4*>(a.scale);
@@ -128,35 +161,81 @@ __global__ void __launch_bounds__(kThreads) row_kernel(const RowArgs a)
     uint4* __restrict__ out = static_cast<uint4*>(a.out);
     const bool has_w = (weight != nullptr);
 
-    int parity = 0;
-    for (int64_t row = static_cast<int64_t>(blockIdx.x) * kGroups + group; row < a.rows;
-         row += static_cast<int64_t>(gridDim.x) * kGroups, parity ^= 1) {
-        const int64_t b = row / a.S;
-        const int64_t base = row * Dv;
+    uint4* wbuf = ring + static_cast<size_t>(warp) * kStages * kNbuf * kSegVec;
+    const uint32_t bar0 = smem_addr(&bars[warp][0]);
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < kStages; ++s)
+            mbar_init(bar0 + 8u * s, 1u);
+        mbar_init_fence();
+    }
+    __syncwarp();
 
-        // ---- load (and for the gated op, form and store the residual stream)
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * kGroups + group;
+    const int64_t step = static_cast<int64_t>(gridDim.x) * kGroups;
+
+    // lane 0 starts the copy of the group's k-th row into stage k % kStages
+    auto issue = [&](int64_t k) {
+        const int64_t row = first + k * step;
+        if (lane != 0 || row >= a.rows)
+            return;
+        const int st = static_cast<int>(k % kStages);
+        const uint32_t bar = bar0 + 8u * st;
+        fence_proxy_async();
+        mbar_expect_tx(bar, kNbuf * seg_bytes);
+        if (seg_bytes) {
+            const uint32_t dst = smem_addr(wbuf + st * kNbuf * kSegVec);
+            bulk_g2s(dst, src0 + row * Dv + s0, seg_bytes, bar);
+            if (kNbuf == 2)
+                bulk_g2s(dst + kSegVec * 16u, src1 + row * Dv + s0, seg_bytes, bar);
+        }
+    };
+#pragma unroll
+    for (int k = 0; k < kStages; ++k)
+        issue(k);
+
+    bool broken = false;  // a copy timed out: keep going (barriers stay matched), skip waits
+    int parity = 0;
+    for (int64_t k = 0; first + k * step < a.rows; ++k, parity ^= 1) {
+        const int64_t row = first + k * step;
+        const int st = static_cast<int>(k % kStages);
+        const uint32_t phase = static_cast<uint32_t>((k / kStages) & 1);
+        if (!broken && !mbar_wait(bar0 + 8u * st, phase, kWaitLimitNs)) {
+            broken = true;
+            if (lane == 0)
+                atomicOr(&g_error, kErrCopyTimeout);
+        }
+        const uint4* b0 = wbuf + st * kNbuf * kSegVec;
+        const int64_t b = row / a.S;
+        const int64_t base = row * Dv + s0;
+
+        // ---- shared -> registers (and for the gated op, form and store the
+        //      residual stream)
         uint4 xv[V];
 #pragma unroll
         for (int j = 0; j < V; ++j) {
-            const int c = j * (32 * WPR) + wig * 32 + lane;
-            if (c < Dv) {
+            const int v = j * 32 + lane;
+            if (v < seg_len) {
                 if (OP == kOpGated) {
-                    uint4 r = ld_stream(residual + base + c);
-                    uint4 u = ld_stream(update + base + c);
-                    uint4 g = ld_cached(gate + b * a.gate_bstride + c);
+                    const uint4 r = b0[v];
+                    const uint4 u = b0[kSegVec + v];
+                    const uint4 g = ld_cached(gate + b * a.gate_bstride + s0 + v);
                     uint4 s;
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         word(s, i) = bf2_add(word(r, i), bf2_mul(word(g, i), word(u, i)));
-                    st_stream(res_out + base + c, s);
+                    st_stream(res_out + base + v, s);
                     xv[j] = s;
                 } else {
-                    xv[j] = ld_stream(x + base + c);
+                    xv[j] = b0[v];
                 }
             } else {
                 xv[j] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
+        // the stage is consumed: refill it with the row kStages ahead
+        __syncwarp();
+        issue(k + kStages);
 
         // ---- magnitude class of this lane's values
         uint32_t m = 0;
@@ -253,17 +332,17 @@ __global__ void __launch_bounds__(kThreads) row_kernel(const RowArgs a)
         // ---- normalise + modulate + store
         const u64 mean2 = f2_splat(mean);
         const u64 rstd2 = f2_splat(rstd);
-        const uint4* sc = scale + b * a.mod_bstride;
-        const uint4* sh = shift + b * a.mod_bstride;
+        const uint4* sc = scale + b * a.mod_bstride + s0;
+        const uint4* sh = shift + b * a.mod_bstride + s0;
 #pragma unroll
         for (int j = 0; j < V; ++j) {
-            const int c = j * (32 * WPR) + wig * 32 + lane;
-            if (c < Dv) {
-                const uint4 s = ld_cached(sc + c);
-                const uint4 h = ld_cached(sh + c);
+            const int v = j * 32 + lane;
+            if (v < seg_len) {
+                const uint4 s = ld_cached(sc + v);
+                const uint4 h = ld_cached(sh + v);
                 uint4 w = make_uint4(0u, 0u, 0u, 0u);
                 if (OP != kOpLN && has_w)
-                    w = ld_cached(weight + c);
+                    w = ld_cached(weight + s0 + v);
                 uint4 o;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -280,30 +359,41 @@ __global__ void __launch_bounds__(kThreads) row_kernel(const RowArgs a)
                     const uint32_t s1 = bf2_add(word(s, i), kBf2One);
                     word(o, i) = bf2_add(bf2_mul(yb, s1), word(h, i));
                 }
-                st_stream(out + base + c, o);
+                st_stream(out + base + v, o);
             }
         }
     }
+    // nothing is left in flight on the normal path (every issued row was
+    // waited for); after a timeout, give outstanding copies a bounded time
+    // to land before the CTA's shared memory is released
+    if (broken)
+        drain_pause();
 }
 
 template <int OP, int V, int WPR>
 cudaError_t launch_cfg(const RowArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
+    using Shape = RowShape<OP, V, WPR>;
     auto kern = row_kernel<OP, V, WPR>;
     static int blocks_per_sm[64] = {0};
-    int d = dev.device & 63;
+    const int d = dev.device & 63;
     if (blocks_per_sm[d] == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Shape::kSmem);
+        if (e != cudaSuccess)
+            return e;
         int n = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Shape::kThreads,
+                                                          Shape::kSmem);
         if (e != cudaSuccess)
             return e;
         blocks_per_sm[d] = n > 0 ? n : 1;
     }
-    constexpr int kGroups = kWarps / WPR;
-    int64_t want = (a.rows + kGroups - 1) / kGroups;
-    int64_t cap = static_cast<int64_t>(dev.sms) * blocks_per_sm[d];
-    int grid = static_cast<int>(want < cap ? want : cap);
-    kern<<<grid, kThreads, 0, stream>>>(a);
+    constexpr int kGroups = Shape::kWarps / WPR;
+    const int64_t want = (a.rows + kGroups - 1) / kGroups;
+    const int64_t cap = static_cast<int64_t>(dev.sms) * blocks_per_sm[d];
+    const int grid = static_cast<int>(want < cap ? want : cap);
+    kern<<<grid, Shape::kThreads, Shape::kSmem, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -341,6 +431,16 @@ cudaError_t launch_row_kernel(int op, const RowArgs& a, const DeviceInfo& dev,
     default:
         return launch_op<kOpGated>(a, dev, stream);
     }
+}
+
+cudaError_t row_kernels_error(unsigned* bits, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(bits, g_error, sizeof(unsigned));
+    if (e == cudaSuccess && clear && *bits) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_error, &zero, sizeof(unsigned));
+    }
+    return e;
 }
 
 }  // namespace rmsmod

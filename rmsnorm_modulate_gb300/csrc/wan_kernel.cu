@@ -5,10 +5,11 @@
 // In a channels_last(_3d) activation each pixel's C channels are contiguous
 // and consecutive pixels are adjacent, so a run of pixels is one contiguous
 // byte range.  P lanes share a pixel (V 16-byte vectors each, P * V * 8 >= C)
-// and a warp covers 32 / P consecutive pixels per step: every warp-wide load
-// instruction reads whole 32-byte sectors of one contiguous span.  A lane's
-// channels never change, so its bias (rounded to bf16 once) and gamma
-// (widened to fp32 once) stay in registers for the whole kernel.
+// and a warp covers 32 / P consecutive pixels per step; that tile is one
+// contiguous span of at most 32 * V vectors, brought into shared memory by a
+// 1-D bulk copy (TMA) into a six-stage ring per warp.  A lane's channels
+// never change, so its bias (rounded to bf16 once) and gamma (widened to
+// fp32 once) stay in registers for the whole kernel.
 //
 //   xb  = R(x + R(bias))              (aten add_ arithmetic, before the statistics)
 //   z   = (xb * rstd) * gamma         (fp32, unrounded)
@@ -20,7 +21,11 @@ namespace rmsmod {
 
 namespace {
 
-constexpr int kThreads = 256;
+__device__ unsigned int g_error;
+
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kStages = 6;
 
 template <int N>
 struct Log2Ceil {
@@ -29,6 +34,12 @@ struct Log2Ceil {
 template <>
 struct Log2Ceil<1> {
     static constexpr int value = 0;
+};
+
+template <int V>
+struct WanShape {
+    static constexpr int kTileVec = 32 * V;  // buffer capacity in 16-byte vectors
+    static constexpr int kSmem = kWarps * kStages * kTileVec * 16;
 };
 
 // SiLU(z) = z * sigmoid(z), sigmoid from e = exp(-|z|) in (0, 1] so nothing
@@ -45,8 +56,11 @@ template <int P, int V>
 __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
 {
     constexpr int kL = Log2Ceil<8 * V>::value;
-    constexpr int kPixPerWarp = 32 / P;
-    constexpr int kPixPerBlock = kPixPerWarp * (kThreads / 32);
+    constexpr int kPix = 32 / P;  // pixels per warp step
+    constexpr int kTileVec = WanShape<V>::kTileVec;
+
+    extern __shared__ __align__(128) uint4 ring[];
+    __shared__ __align__(8) unsigned long long bars[kWarps][kStages];
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -85,18 +99,56 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
         }
     }
 
-    for (int64_t pix0 = (static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp) * kPixPerWarp;
-         pix0 < a.pixels; pix0 += static_cast<int64_t>(gridDim.x) * kPixPerBlock) {
+    uint4* wbuf = ring + warp * kStages * kTileVec;
+    const uint32_t bar0 = smem_addr(&bars[warp][0]);
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < kStages; ++s)
+            mbar_init(bar0 + 8u * s, 1u);
+        mbar_init_fence();
+    }
+    __syncwarp();
+
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarps + warp;  // tile index
+    const int64_t step = static_cast<int64_t>(gridDim.x) * kWarps;
+    auto issue = [&](int64_t k) {
+        const int64_t pix0 = (first + k * step) * kPix;
+        if (lane != 0 || pix0 >= a.pixels)
+            return;
+        const int64_t left = a.pixels - pix0;
+        const uint32_t bytes =
+            static_cast<uint32_t>((left < kPix ? left : kPix) * Cv) * 16u;
+        const int st = static_cast<int>(k % kStages);
+        const uint32_t bar = bar0 + 8u * st;
+        fence_proxy_async();
+        mbar_expect_tx(bar, bytes);
+        bulk_g2s(smem_addr(wbuf + st * kTileVec), x + pix0 * Cv, bytes, bar);
+    };
+#pragma unroll
+    for (int k = 0; k < kStages; ++k)
+        issue(k);
+
+    bool broken = false;
+    for (int64_t k = 0; (first + k * step) * kPix < a.pixels; ++k) {
+        const int64_t pix0 = (first + k * step) * kPix;
+        const int st = static_cast<int>(k % kStages);
+        if (!broken && !mbar_wait(bar0 + 8u * st, static_cast<uint32_t>((k / kStages) & 1),
+                                  kWaitLimitNs)) {
+            broken = true;
+            if (lane == 0)
+                atomicOr(&g_error, kErrCopyTimeout);
+        }
         const int64_t pix = pix0 + psub;
         const bool valid = pix < a.pixels;
         const int64_t base = pix * Cv;
 
+        const uint4* tile = wbuf + st * kTileVec + psub * Cv;
         uint4 xv[V];
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int c = sub + P * j;
             if (valid && c < Cv) {
-                uint4 v = ld_stream(x + base + c);
+                uint4 v = tile[c];
                 if (has_bias) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
@@ -107,6 +159,8 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
                 xv[j] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
+        __syncwarp();
+        issue(k + kStages);
 
         uint32_t m = 0;
 #pragma unroll
@@ -179,26 +233,33 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
             }
         }
     }
+    if (broken)
+        drain_pause();
 }
 
 template <int P, int V>
 cudaError_t launch_cfg(const WanArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
     auto kern = wan_kernel<P, V>;
+    constexpr int kSmem = WanShape<V>::kSmem;
     static int blocks_per_sm[64] = {0};
     const int d = dev.device & 63;
     if (blocks_per_sm[d] == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmem);
+        if (e != cudaSuccess)
+            return e;
         int nb = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads, 0);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads, kSmem);
         if (e != cudaSuccess)
             return e;
         blocks_per_sm[d] = nb > 0 ? nb : 1;
     }
-    constexpr int kPixPerBlock = (32 / P) * (kThreads / 32);
+    constexpr int kPixPerBlock = (32 / P) * kWarps;
     const int64_t want = (a.pixels + kPixPerBlock - 1) / kPixPerBlock;
     const int64_t cap = static_cast<int64_t>(dev.sms) * blocks_per_sm[d];
     const int grid = static_cast<int>(want < cap ? want : cap);
-    kern<<<grid, kThreads, 0, stream>>>(a);
+    kern<<<grid, kThreads, kSmem, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -237,6 +298,16 @@ cudaError_t launch_wan_kernel(const WanArgs& a, const DeviceInfo& dev, cudaStrea
     if (need <= 16)
         return launch_p<16>(a, dev, stream);
     return launch_p<32>(a, dev, stream);
+}
+
+cudaError_t wan_kernel_error(unsigned* bits, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(bits, g_error, sizeof(unsigned));
+    if (e == cudaSuccess && clear && *bits) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_error, &zero, sizeof(unsigned));
+    }
+    return e;
 }
 
 }  // namespace rmsmod

@@ -20,7 +20,8 @@ pytestmark = pytest.mark.gpu
 def rm():
     import rmsnorm_modulate_gb300 as rm
 
-    return rm
+    yield rm
+    assert rm.device_status(clear=True) == 0
 
 
 def same_bits(a, b):

@@ -10,7 +10,7 @@ import torch
 
 import workloads as W
 from _gpu import dev, host, stat_report
-from _util import assert_within_ulp
+from _util import assert_exact_where_stats_match, assert_within_ulp
 
 pytestmark = pytest.mark.gpu
 
@@ -19,7 +19,8 @@ pytestmark = pytest.mark.gpu
 def rm():
     import rmsnorm_modulate_gb300 as rm
 
-    return rm
+    yield rm
+    assert rm.device_status(clear=True) == 0
 
 
 def run_ln(rm, oracle_mod, inp, eps=1e-6, check_stats=True):
@@ -35,6 +36,8 @@ def run_ln(rm, oracle_mod, inp, eps=1e-6, check_stats=True):
         fr, wr = stat_report(host(rstd), o_rstd)
         assert wm <= 1e-5 and wr <= 1e-5, (wm, wr)
     d = assert_within_ulp(host(out), o_out)
+    assert_exact_where_stats_match(host(out), o_out, inp["D"], (host(mean), o_mean),
+                                   (host(rstd), o_rstd), min_match=0.99 if check_stats else 0)
     return d, host(mean), host(rstd), o_mean, o_rstd
 
 

@@ -5,7 +5,7 @@ import torch
 
 import workloads as W
 from _gpu import dev, host, stat_report
-from _util import assert_within_ulp
+from _util import assert_exact_where_stats_match, assert_within_ulp
 
 pytestmark = pytest.mark.gpu
 
@@ -14,7 +14,8 @@ pytestmark = pytest.mark.gpu
 def rm():
     import rmsnorm_modulate_gb300 as rm
 
-    return rm
+    yield rm
+    assert rm.device_status(clear=True) == 0
 
 
 def run_qk(rm, oracle_mod, inp, eps=1e-5):
@@ -30,6 +31,9 @@ def run_qk(rm, oracle_mod, inp, eps=1e-5):
     assert stat_report(host(rstd), orr)[1] <= 1e-5
     dq = assert_within_ulp(host(qo), oq, what="q")
     dk = assert_within_ulp(host(ko), ok, what="k")
+    gm, gr = host(mean), host(rstd)
+    assert_exact_where_stats_match(host(qo), oq, 128, (gm[:rq], om[:rq]), (gr[:rq], orr[:rq]))
+    assert_exact_where_stats_match(host(ko), ok, 128, (gm[rq:], om[rq:]), (gr[rq:], orr[rq:]))
     return dq, dk, host(mean), host(rstd), om, orr
 
 
@@ -63,3 +67,7 @@ def test_edge_and_special_rows(rm, oracle_mod):
     assert_within_ulp(host(ko), ok)
     g = host(rstd)
     assert np.all((g == orr) | (np.isnan(g) & np.isnan(orr)))
+    gm = host(mean)
+    assert_exact_where_stats_match(host(qo), oq, 128, (gm[:rq], om[:rq]), (g[:rq], orr[:rq]))
+    assert_exact_where_stats_match(host(ko), ok, 128, (gm[rq:], om[rq:]), (g[rq:], orr[rq:]),
+                                   min_match=0)

@@ -7,7 +7,7 @@ import torch
 
 import workloads as W
 from _gpu import dev, host, stat_report
-from _util import assert_within_ulp
+from _util import assert_exact_where_stats_match, assert_within_ulp
 
 pytestmark = pytest.mark.gpu
 
@@ -16,7 +16,8 @@ pytestmark = pytest.mark.gpu
 def rm():
     import rmsnorm_modulate_gb300 as rm
 
-    return rm
+    yield rm
+    assert rm.device_status(clear=True) == 0
 
 
 def run_rms(rm, oracle_mod, inp, eps=1e-6):
@@ -31,6 +32,7 @@ def run_rms(rm, oracle_mod, inp, eps=1e-6):
     frac, worst = stat_report(host(rstd), o_rstd)
     assert worst <= 1e-5
     d = assert_within_ulp(host(out), o_out)
+    assert_exact_where_stats_match(host(out), o_out, inp["D"], (host(rstd), o_rstd))
     return d, host(rstd), o_rstd
 
 
@@ -49,6 +51,7 @@ def run_gated(rm, oracle_mod, inp, eps=1e-6):
     frac, worst = stat_report(host(rstd), o_rstd)
     assert worst <= 1e-5
     d = assert_within_ulp(host(out), o_out)
+    assert_exact_where_stats_match(host(out), o_out, inp["D"], (host(rstd), o_rstd))
     return d, host(rstd), o_rstd
 
 
@@ -109,6 +112,7 @@ def test_rms_edge_and_special_rows(rm, oracle_mod):
             for i, l in enumerate(labels):
                 assert g[i] == o_rstd[i] or (np.isnan(g[i]) and np.isnan(o_rstd[i])), (D, l)
             assert_within_ulp(host(out), o_out)
+            assert_exact_where_stats_match(host(out), o_out, D, (g, o_rstd), min_match=0)
 
 
 def test_gated_in_place_residual(rm, oracle_mod):

@@ -18,7 +18,8 @@ pytestmark = pytest.mark.gpu
 def rm():
     import rmsnorm_modulate_gb300 as rm
 
-    return rm
+    yield rm
+    assert rm.device_status(clear=True) == 0
 
 
 def run_wan(rm, oracle_mod, inp, eps=1e-6, max_ulp=1):

@@ -216,6 +216,12 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi)
 
 constexpr uint32_t kBf2One = 0x3F803F80u;  // (1.0, 1.0)
 
+// R(f(v) + f(c)) for the eight bf16 of a vector against a bf16x2 constant.
+__device__ __forceinline__ uint4 bf2x4_add(uint4 v, uint32_t c)
+{
+    return make_uint4(bf2_add(v.x, c), bf2_add(v.y, c), bf2_add(v.z, c), bf2_add(v.w, c));
+}
+
 // ---------------------------------------------------------------------------
 // f32x2 (two fp32 in one 64-bit register pair)
 // ---------------------------------------------------------------------------
@@ -394,7 +400,8 @@ __device__ __forceinline__ float offset_k2(uint32_t E)
     return __uint_as_float((2u * E - 124u + L) << 23);
 }
 
-// Accumulator for sum x (optional) and sum x^2.
+// Accumulator for sum x (optional) and sum x^2.  Each f32x2 register holds
+// two independent accumulators (even / odd elements).
 template <bool NEED_SUM>
 struct ExactSums {
     u64 acc1, err1, acc2, err2, k1, k2;
@@ -412,14 +419,16 @@ struct ExactSums {
     __device__ __forceinline__ void add(u64 xx)
     {
         if (NEED_SUM) {
-            u64 s = f2_add(acc1, xx);
-            u64 z = f2_sub(s, acc1);
+            const u64 s = f2_add(acc1, xx);
+            const u64 z = f2_sub(s, acc1);
             err1 = f2_add(err1, f2_sub(xx, z));
             acc1 = s;
         }
-        u64 s2 = f2_fma(xx, xx, acc2);
-        u64 z2 = f2_sub(s2, acc2);
-        err2 = f2_add(err2, f2_fma(xx, xx, f2_neg(z2)));
+        // s2 = acc + x^2 rounded; acc - s2 is exact (Sterbenz), so the
+        // rounding error x^2 - (s2 - acc) is one more FMA with no negation
+        const u64 s2 = f2_fma(xx, xx, acc2);
+        const u64 zn = f2_sub(acc2, s2);
+        err2 = f2_add(err2, f2_fma(xx, xx, zn));
         acc2 = s2;
     }
 
@@ -427,19 +436,35 @@ struct ExactSums {
     __device__ __forceinline__ void lane_total(float& s1h, float& s1l, float& s2h, float& s2l)
     {
         // halves: h = acc - K exact, l = err
-        u64 h1 = f2_sub(acc1, k1), h2 = f2_sub(acc2, k2);
+        const u64 h1 = f2_sub(acc1, k1), h2 = f2_sub(acc2, k2);
         float a0, a1, b0, b1, c0, c1, d0, d1;
         f2_unpack(h1, a0, a1);
         f2_unpack(err1, b0, b1);
         f2_unpack(h2, c0, c1);
         f2_unpack(err2, d0, d1);
-        // combine even/odd halves: (a0 + b0) + (a1 + b1), (c0 + d0) + (c1 + d1)
+        // even + odd halves: (a0 + b0) + (a1 + b1), (c0 + d0) + (c1 + d1)
         u64 H = f2_pack(a0, c0), Lo = f2_pack(b0, d0);
         dd2_add(H, Lo, f2_pack(a1, c1), f2_pack(b1, d1));
         f2_unpack(H, s1h, s2h);
         f2_unpack(Lo, s1l, s2l);
     }
 };
+
+// Largest |x| bits over V vectors, as a balanced tree (short dependency chain).
+template <int V>
+__device__ __forceinline__ uint32_t tree_absmax(const uint4 (&xv)[V])
+{
+    uint32_t m[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j)
+        m[j] = bf2_absmax(bf2_absmax(xv[j].x, xv[j].y), bf2_absmax(xv[j].z, xv[j].w));
+#pragma unroll
+    for (int w = 1; w < V; w *= 2)
+#pragma unroll
+        for (int j = 0; j + w < V; j += 2 * w)
+            m[j] = bf2_absmax(m[j], m[j + w]);
+    return absmax_bits(m[0]);
+}
 
 // Butterfly over `width` lanes (power of two) of two double-floats at once;
 // every participating lane ends with the total.
@@ -520,6 +545,24 @@ __device__ __forceinline__ void finalize_ln(float s1h, float s1l, float s2h, flo
     nl = __fsub_rn(q2, __fsub_rn(nh, q1));
     dd_div_n(nh, nl, n, inv_n, q1, q2);
     var = __fadd_rn(q1, q2);
+    var = var > 0.0f ? var : 0.0f;
+}
+
+// finalize_ln for a power-of-two n (inv_n exact): the divisions become exact
+// scalings, so only the two roundings to fp32 remain.
+__device__ __forceinline__ void finalize_ln_pow2(float s1h, float s1l, float s2h, float s2l,
+                                                 float n, float inv_n, float& mean, float& var)
+{
+    mean = __fmul_rn(__fadd_rn(s1h, s1l), inv_n);
+    const float p1 = __fmul_rn(n, s2h);  // exact
+    const float p2 = __fmul_rn(s1h, s1h);
+    const float e2 = __fmaf_rn(s1h, s1h, -p2);
+    const float s = __fsub_rn(p1, p2);
+    const float v = __fsub_rn(s, p1);
+    float e = __fadd_rn(__fsub_rn(p1, __fsub_rn(s, v)), __fsub_rn(-p2, v));
+    const float cross = __fmaf_rn(n, s2l, -__fmul_rn(__fmul_rn(2.0f, s1h), s1l));
+    e = __fadd_rn(e, __fsub_rn(cross, e2));
+    var = __fmul_rn(__fmul_rn(__fadd_rn(s, e), inv_n), inv_n);
     var = var > 0.0f ? var : 0.0f;
 }
 

@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blo
         uint32_t emax = allreduce_max<kLanesPerRow>(mm == 0 ? 0u : (mm >> 7));
 
         float mean, var;
-        finalize_ln(s1h, s1l, s2h, s2l, n, inv_n, mean, var);
+        finalize_ln_pow2(s1h, s1l, s2h, s2l, n, inv_n, mean, var);
         if (__any_sync(kFullMask, cls != kClassFast)) {
             // Rare: some row of this tile holds Inf/NaN or extreme magnitudes.
             // Every lane runs both slow variants (warp-uniform control flow)
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blo
                 var = __fsub_rn(__fmul_rn(p2, inv_n), __fmul_rn(mean, mean));
             } else if (cls == kClassScaled) {
                 float ms, vs;
-                finalize_ln(t1h, t1l, t2h, t2l, n, inv_n, ms, vs);
+                finalize_ln_pow2(t1h, t1l, t2h, t2l, n, inv_n, ms, vs);
                 mean = rs.unscale(ms, 1);
                 var = rs.unscale(vs, 2);
             }

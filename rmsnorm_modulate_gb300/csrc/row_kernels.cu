@@ -104,25 +104,130 @@ __device__ __forceinline__ void group_sum_plain(Slot* slots, int wig, int lane, 
     group_barrier<WPR>(group);
 }
 
+// Statistics of a row that holds Inf/NaN (plain IEEE sums, which propagate
+// them the way the exact double sums do) or extreme magnitudes (scaled to
+// unit size by a power of two, exact sums, scaled back).  Group-uniform.
+template <bool kNeedSum, int V, int WPR, int kL>
+__device__ __noinline__ void slow_stats(const uint4 (&xv)[V], uint32_t cls, uint32_t emax,
+                                        Slot* slots, int wig, int lane, int group, float n,
+                                        float inv_n, float& mean, float& stat)
+{
+    if (cls == kClassNonFinite) {
+        float p1 = 0.0f, p2 = 0.0f;
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float lo, hi;
+                f2_unpack(f2_from_bf2(word(xv[j], i)), lo, hi);
+                p1 = __fadd_rn(__fadd_rn(p1, lo), hi);
+                p2 = __fadd_rn(__fadd_rn(p2, __fmul_rn(lo, lo)), __fmul_rn(hi, hi));
+            }
+        p1 = allreduce_add<32>(p1);
+        p2 = allreduce_add<32>(p2);
+        group_sum_plain<WPR>(slots, wig, lane, group, p1, p2);
+        mean = __fmul_rn(p1, inv_n);
+        const float msq = __fmul_rn(p2, inv_n);
+        stat = kNeedSum ? __fsub_rn(msq, __fmul_rn(mean, mean)) : msq;
+        return;
+    }
+    RowScale rs;
+    rs.set(emax);
+    ExactSums<kNeedSum> acc2;
+    acc2.init(offset_k1<kL>(127u), offset_k2<kL>(127u));
+#pragma unroll
+    for (int j = 0; j < V; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            acc2.add(rs.apply(f2_from_bf2(word(xv[j], i))));
+    float s1h, s1l, s2h, s2l;
+    acc2.lane_total(s1h, s1l, s2h, s2l);
+    if (kNeedSum)
+        dd2_allreduce<32>(s1h, s1l, s2h, s2l);
+    else
+        dd_allreduce<32>(s2h, s2l);
+    uint32_t c2 = cls, e2 = emax;
+    group_combine<WPR>(slots, wig, lane, group, s1h, s1l, s2h, s2l, c2, e2);
+    group_barrier<WPR>(group);
+    if (kNeedSum) {
+        float ms, vs;
+        finalize_ln(s1h, s1l, s2h, s2l, n, inv_n, ms, vs);
+        mean = rs.unscale(ms, 1);
+        stat = rs.unscale(vs, 2);
+    } else {
+        mean = 0.0f;
+        stat = rs.unscale(finalize_ms(s2h, s2l, n, inv_n), 2);
+    }
+}
+
 // Compile-time shape of one kernel instance.
 template <int OP, int V, int WPR>
 struct RowShape {
-    static constexpr int kStages = 2;
+    static constexpr int kStages = V >= 8 ? 1 : 2;  // rows in flight per warp
     static constexpr int kNbuf = (OP == kOpGated) ? 2 : 1;   // residual + update
     static constexpr int kSegVec = 32 * V;                   // 16-byte vectors per buffer
     static constexpr int kWarpBytes = kStages * kNbuf * kSegVec * 16;
-    // as many warps as ~96 KB of ring allows (two CTAs per SM), at most 8,
-    // a multiple of WPR
-    static constexpr int kFit = (96 * 1024) / kWarpBytes;
-    static constexpr int kWarps0 = kFit > 8 ? 8 : (kFit < 1 ? 1 : kFit);
+    // Rows of up to 4096 values keep the per-row re-read vectors in shared
+    // memory: R(1 + scale) and shift, plus weight (RMS) and gate (gated).
+    static constexpr bool kCached = 32 * V * WPR <= 512;
+    static constexpr int kNmod = OP == kOpLN ? 2 : (OP == kOpRMS ? 3 : 4);
+    static constexpr int kCacheBytes = kCached ? kNmod * 32 * V * WPR * 16 : 0;
+    // as many warps as ~108 KB per CTA allows, a multiple of WPR; at most 8,
+    // or 6 for the larger per-lane rows so three CTAs per SM keep ~110
+    // registers per thread
+    // registers bound the resident rows: 8 warps x 2 CTAs (128 registers) up
+    // to 12 vectors per lane, 6 warps x 2 CTAs (170) for 16
+    static constexpr int kMaxWarps = V >= 16 ? 6 : 8;
+    static constexpr int kFit = (108 * 1024 - kCacheBytes) / kWarpBytes;
+    static constexpr int kWarps0 = kFit > kMaxWarps ? kMaxWarps : (kFit < 1 ? 1 : kFit);
     static constexpr int kWarps = (kWarps0 / WPR) * WPR < WPR ? WPR : (kWarps0 / WPR) * WPR;
     static constexpr int kThreads = 32 * kWarps;
-    static constexpr int kSmem = kWarps * kWarpBytes;
+    static constexpr int kRingBytes = kWarps * kWarpBytes;
+    // CTAs per SM the shared memory allows (the register budget follows it)
+    static constexpr int kSmemPerCta = kRingBytes + kCacheBytes + 2048;
+    static constexpr int kBlocks0 = (224 * 1024) / kSmemPerCta;
+    static constexpr int kBlockCap = V >= 8 ? 2 : 3;
+    static constexpr int kBlocks = kBlocks0 > kBlockCap ? kBlockCap : (kBlocks0 < 1 ? 1 : kBlocks0);
 };
 
-template <int OP, int V, int WPR>
-__global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads)
-    row_kernel(const RowArgs a)
+// out = R(R(y * s1) + shift) for one 16-byte vector, y from x and the row's
+// statistics: the normalise step and the modulate chain.
+template <int OP>
+__device__ __forceinline__ uint4 normalise_modulate(const uint4& xv, u64 mean2, u64 rstd2,
+                                                    const uint4& s1, const uint4& sh,
+                                                    const uint4& w, bool has_w)
+{
+    uint4 o;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const u64 xx = f2_from_bf2(word(xv, i));
+        u64 y;
+        if (OP == kOpLN) {
+            y = f2_mul(f2_sub(xx, mean2), rstd2);
+        } else {
+            y = f2_mul(xx, rstd2);
+            if (has_w)
+                y = f2_mul(y, f2_from_bf2(word(w, i)));
+        }
+        word(o, i) = bf2_add(bf2_mul(bf2_from_f2(y), word(s1, i)), word(sh, i));
+    }
+    return o;
+}
+
+// Work is split into items: a contiguous range of rows of one batch, so an
+// item needs one set of modulation rows.  A CTA takes items blockIdx.x,
+// blockIdx.x + gridDim.x, ...; its row groups take the item's rows in turn.
+struct Items {
+    int64_t per_batch;  // items per batch
+    int64_t chunk;      // rows per item (the last item of a batch may be shorter)
+    int64_t count;
+};
+
+// EXACT: every warp segment is exactly 32 * V vectors (D = 256 * V * WPR),
+// so no vector needs a bounds check.
+template <int OP, int V, int WPR, bool EXACT>
+__global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads, RowShape<OP, V, WPR>::kBlocks)
+    row_kernel(const RowArgs a, const Items items)
 {
     using Shape = RowShape<OP, V, WPR>;
     constexpr int kWarps = Shape::kWarps;
@@ -130,6 +235,7 @@ __global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads)
     constexpr int kStages = Shape::kStages;
     constexpr int kNbuf = Shape::kNbuf;
     constexpr int kSegVec = Shape::kSegVec;
+    constexpr bool kCached = Shape::kCached;
     constexpr int kL = Log2Ceil<8 * V>::value;
     constexpr bool kNeedSum = (OP == kOpLN);
 
@@ -161,6 +267,13 @@ __global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads)
     uint4* __restrict__ out = static_cast<uint4*>(a.out);
     const bool has_w = (weight != nullptr);
 
+    // modulation rows of the current item's batch (kCached only)
+    uint4* cache = ring + Shape::kRingBytes / 16;
+    uint4* c_s1 = cache;
+    uint4* c_sh = cache + Dv;
+    uint4* c_w = cache + 2 * Dv;
+    uint4* c_g = cache + 3 * Dv;
+
     uint4* wbuf = ring + static_cast<size_t>(warp) * kStages * kNbuf * kSegVec;
     const uint32_t bar0 = smem_addr(&bars[warp][0]);
     if (lane == 0) {
@@ -171,197 +284,158 @@ __global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads)
     }
     __syncwarp();
 
-    const int64_t first = static_cast<int64_t>(blockIdx.x) * kGroups + group;
-    const int64_t step = static_cast<int64_t>(gridDim.x) * kGroups;
-
-    // lane 0 starts the copy of the group's k-th row into stage k % kStages
-    auto issue = [&](int64_t k) {
-        const int64_t row = first + k * step;
-        if (lane != 0 || row >= a.rows)
-            return;
-        const int st = static_cast<int>(k % kStages);
-        const uint32_t bar = bar0 + 8u * st;
-        fence_proxy_async();
-        mbar_expect_tx(bar, kNbuf * seg_bytes);
-        if (seg_bytes) {
-            const uint32_t dst = smem_addr(wbuf + st * kNbuf * kSegVec);
-            bulk_g2s(dst, src0 + row * Dv + s0, seg_bytes, bar);
-            if (kNbuf == 2)
-                bulk_g2s(dst + kSegVec * 16u, src1 + row * Dv + s0, seg_bytes, bar);
-        }
-    };
-#pragma unroll
-    for (int k = 0; k < kStages; ++k)
-        issue(k);
-
     bool broken = false;  // a copy timed out: keep going (barriers stay matched), skip waits
     int parity = 0;
-    for (int64_t k = 0; first + k * step < a.rows; ++k, parity ^= 1) {
-        const int64_t row = first + k * step;
-        const int st = static_cast<int>(k % kStages);
-        const uint32_t phase = static_cast<uint32_t>((k / kStages) & 1);
-        if (!broken && !mbar_wait(bar0 + 8u * st, phase, kWaitLimitNs)) {
-            broken = true;
-            if (lane == 0)
-                atomicOr(&g_error, kErrCopyTimeout);
-        }
-        const uint4* b0 = wbuf + st * kNbuf * kSegVec;
-        const int64_t b = row / a.S;
-        const int64_t base = row * Dv + s0;
+    int64_t uses = 0;     // rows this warp has run through its ring
 
-        // ---- shared -> registers (and for the gated op, form and store the
-        //      residual stream)
-        uint4 xv[V];
-#pragma unroll
-        for (int j = 0; j < V; ++j) {
-            const int v = j * 32 + lane;
-            if (v < seg_len) {
-                if (OP == kOpGated) {
-                    const uint4 r = b0[v];
-                    const uint4 u = b0[kSegVec + v];
-                    const uint4 g = ld_cached(gate + b * a.gate_bstride + s0 + v);
-                    uint4 s;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        word(s, i) = bf2_add(word(r, i), bf2_mul(word(g, i), word(u, i)));
-                    st_stream(res_out + base + v, s);
-                    xv[j] = s;
-                } else {
-                    xv[j] = b0[v];
-                }
-            } else {
-                xv[j] = make_uint4(0u, 0u, 0u, 0u);
+    for (int64_t item = blockIdx.x; item < items.count; item += gridDim.x) {
+        const int64_t b = item / items.per_batch;
+        const int64_t r_begin = b * a.S + (item % items.per_batch) * items.chunk;
+        const int64_t r_lim = (b + 1) * a.S;
+        const int64_t r_end = r_begin + items.chunk < r_lim ? r_begin + items.chunk : r_lim;
+
+        // lane 0 starts the copy of this group's k-th row of the item into
+        // its ring (use counter uses + k)
+        auto issue = [&](int64_t k) {
+            const int64_t row = r_begin + group + k * kGroups;
+            if (lane != 0 || row >= r_end)
+                return;
+            const int st = static_cast<int>((uses + k) % kStages);
+            const uint32_t bar = bar0 + 8u * st;
+            fence_proxy_async();
+            mbar_expect_tx(bar, kNbuf * seg_bytes);
+            if (seg_bytes) {
+                const uint32_t dst = smem_addr(wbuf + st * kNbuf * kSegVec);
+                bulk_g2s(dst, src0 + row * Dv + s0, seg_bytes, bar);
+                if (kNbuf == 2)
+                    bulk_g2s(dst + kSegVec * 16u, src1 + row * Dv + s0, seg_bytes, bar);
             }
+        };
+#pragma unroll
+        for (int k = 0; k < kStages; ++k)
+            issue(k);
+
+        if (kCached) {
+            __syncthreads();  // every group is done with the previous item's rows
+            for (int c = threadIdx.x; c < Dv; c += blockDim.x) {
+                c_s1[c] = bf2x4_add(ld_cached(scale + b * a.mod_bstride + c), kBf2One);
+                c_sh[c] = ld_cached(shift + b * a.mod_bstride + c);
+                if (OP != kOpLN && has_w)
+                    c_w[c] = ld_cached(weight + c);
+                if (OP == kOpGated)
+                    c_g[c] = ld_cached(gate + b * a.gate_bstride + c);
+            }
+            __syncthreads();
         }
-        // the stage is consumed: refill it with the row kStages ahead
-        __syncwarp();
-        issue(k + kStages);
 
-        // ---- magnitude class of this lane's values
-        uint32_t m = 0;
-#pragma unroll
-        for (int j = 0; j < V; ++j)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                m = bf2_absmax(m, word(xv[j], i));
-        const uint32_t mm = absmax_bits(m);
-        const uint32_t E = offset_exponent(mm);
+        int64_t k = 0;
+        for (int64_t row = r_begin + group; row < r_end; row += kGroups, ++k, parity ^= 1) {
+            const int st = static_cast<int>((uses + k) % kStages);
+            const uint32_t phase = static_cast<uint32_t>(((uses + k) / kStages) & 1);
+            if (!broken && !mbar_wait(bar0 + 8u * st, phase, kWaitLimitNs)) {
+                broken = true;
+                if (lane == 0)
+                    atomicOr(&g_error, kErrCopyTimeout);
+            }
+            const uint4* b0 = wbuf + st * kNbuf * kSegVec;
+            const int64_t base = row * Dv + s0;
 
-        // ---- exact sums (fast path; discarded if the row needs the slow path)
-        ExactSums<kNeedSum> acc;
-        acc.init(offset_k1<kL>(E), offset_k2<kL>(E));
+            // ---- shared -> registers (and for the gated op, form and store
+            //      the residual stream)
+            uint4 xv[V];
 #pragma unroll
-        for (int j = 0; j < V; ++j)
+            for (int j = 0; j < V; ++j) {
+                const int v = j * 32 + lane;
+                if (EXACT || v < seg_len) {
+                    if (OP == kOpGated) {
+                        const uint4 r = b0[v];
+                        const uint4 u = b0[kSegVec + v];
+                        const uint4 g = kCached ? c_g[s0 + v]
+                                                : ld_cached(gate + b * a.gate_bstride + s0 + v);
+                        uint4 s;
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                acc.add(f2_from_bf2(word(xv[j], i)));
-        float s1h, s1l, s2h, s2l;
-        acc.lane_total(s1h, s1l, s2h, s2l);
-        if (kNeedSum)
-            dd2_allreduce<32>(s1h, s1l, s2h, s2l);
-        else
-            dd_allreduce<32>(s2h, s2l);
-        uint32_t cls = __reduce_max_sync(kFullMask, static_cast<uint32_t>(magnitude_class(mm)));
-        uint32_t emax = __reduce_max_sync(kFullMask, mm == 0 ? 0u : (mm >> 7));
-        group_combine<WPR>(&slots[parity][group][0], wig, lane, group, s1h, s1l, s2h, s2l,
-                           cls, emax);
-
-        float mean = 0.0f, stat;
-        if (cls == kClassFast) {
-            if (kNeedSum)
-                finalize_ln(s1h, s1l, s2h, s2l, a.n, a.inv_n, mean, stat);
-            else
-                stat = finalize_ms(s2h, s2l, a.n, a.inv_n);
-        } else if (cls == kClassNonFinite) {
-            // Inf / NaN in the row: plain IEEE sums propagate them the way
-            // the exact (double) sums do.
-            float p1 = 0.0f, p2 = 0.0f;
-#pragma unroll
-            for (int j = 0; j < V; ++j)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float lo, hi;
-                    f2_unpack(f2_from_bf2(word(xv[j], i)), lo, hi);
-                    p1 = __fadd_rn(__fadd_rn(p1, lo), hi);
-                    p2 = __fadd_rn(__fadd_rn(p2, __fmul_rn(lo, lo)), __fmul_rn(hi, hi));
+                        for (int i = 0; i < 4; ++i)
+                            word(s, i) = bf2_add(word(r, i), bf2_mul(word(g, i), word(u, i)));
+                        st_stream(res_out + base + v, s);
+                        xv[j] = s;
+                    } else {
+                        xv[j] = b0[v];
+                    }
+                } else {
+                    xv[j] = make_uint4(0u, 0u, 0u, 0u);
                 }
-            p1 = allreduce_add<32>(p1);
-            p2 = allreduce_add<32>(p2);
-            group_sum_plain<WPR>(&slow_slots[group][0], wig, lane, group, p1, p2);
-            mean = __fmul_rn(p1, a.inv_n);
-            const float msq = __fmul_rn(p2, a.inv_n);
-            stat = kNeedSum ? __fsub_rn(msq, __fmul_rn(mean, mean)) : msq;
-        } else {
-            // Extreme magnitudes: scale the row to unit size by a power of
-            // two (exact), sum, and scale the statistics back.
-            RowScale rs;
-            rs.set(emax);
-            ExactSums<kNeedSum> acc2;
-            acc2.init(offset_k1<kL>(127u), offset_k2<kL>(127u));
+            }
+            // the stage is consumed: refill it with the row kStages ahead
+            __syncwarp();
+            issue(k + kStages);
+
+            // ---- magnitude class of this lane's values
+            const uint32_t mm = tree_absmax<V>(xv);
+            const uint32_t E = offset_exponent(mm);
+
+            // ---- exact sums (fast path; discarded if the row needs the slow path)
+            ExactSums<kNeedSum> acc;
+            acc.init(offset_k1<kL>(E), offset_k2<kL>(E));
 #pragma unroll
             for (int j = 0; j < V; ++j)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    acc2.add(rs.apply(f2_from_bf2(word(xv[j], i))));
-            acc2.lane_total(s1h, s1l, s2h, s2l);
+                    acc.add(f2_from_bf2(word(xv[j], i)));
+            float s1h, s1l, s2h, s2l;
+            acc.lane_total(s1h, s1l, s2h, s2l);
             if (kNeedSum)
                 dd2_allreduce<32>(s1h, s1l, s2h, s2l);
             else
                 dd_allreduce<32>(s2h, s2l);
-            uint32_t c2 = cls, e2 = emax;
-            group_combine<WPR>(&slow_slots[group][0], wig, lane, group, s1h, s1l, s2h, s2l, c2,
-                               e2);
-            group_barrier<WPR>(group);
-            if (kNeedSum) {
-                float ms, vs;
-                finalize_ln(s1h, s1l, s2h, s2l, a.n, a.inv_n, ms, vs);
-                mean = rs.unscale(ms, 1);
-                stat = rs.unscale(vs, 2);
-            } else {
-                stat = rs.unscale(finalize_ms(s2h, s2l, a.n, a.inv_n), 2);
-            }
-        }
-        const float rstd = rstd_from(stat, a.eps);
-        if (lane == 0 && wig == 0) {
-            if (a.mean_out)
-                a.mean_out[row] = mean;
-            if (a.rstd_out)
-                a.rstd_out[row] = rstd;
-        }
+            uint32_t cls =
+                __reduce_max_sync(kFullMask, static_cast<uint32_t>(magnitude_class(mm)));
+            uint32_t emax = __reduce_max_sync(kFullMask, mm == 0 ? 0u : (mm >> 7));
+            group_combine<WPR>(&slots[parity][group][0], wig, lane, group, s1h, s1l, s2h, s2l,
+                               cls, emax);
 
-        // ---- normalise + modulate + store
-        const u64 mean2 = f2_splat(mean);
-        const u64 rstd2 = f2_splat(rstd);
-        const uint4* sc = scale + b * a.mod_bstride + s0;
-        const uint4* sh = shift + b * a.mod_bstride + s0;
+            float mean = 0.0f, stat;
+            if (cls == kClassFast) {
+                if (kNeedSum)
+                    finalize_ln(s1h, s1l, s2h, s2l, a.n, a.inv_n, mean, stat);
+                else
+                    stat = finalize_ms(s2h, s2l, a.n, a.inv_n);
+            } else {
+                slow_stats<kNeedSum, V, WPR, kL>(xv, cls, emax, &slow_slots[group][0], wig, lane,
+                                                 group, a.n, a.inv_n, mean, stat);
+            }
+            const float rstd = rstd_from(stat, a.eps);
+            if (lane == 0 && wig == 0) {
+                if (a.mean_out)
+                    a.mean_out[row] = mean;
+                if (a.rstd_out)
+                    a.rstd_out[row] = rstd;
+            }
+
+            // ---- normalise + modulate + store
+            const u64 mean2 = f2_splat(mean);
+            const u64 rstd2 = f2_splat(rstd);
 #pragma unroll
-        for (int j = 0; j < V; ++j) {
-            const int v = j * 32 + lane;
-            if (v < seg_len) {
-                const uint4 s = ld_cached(sc + v);
-                const uint4 h = ld_cached(sh + v);
-                uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                if (OP != kOpLN && has_w)
-                    w = ld_cached(weight + s0 + v);
-                uint4 o;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const u64 xx = f2_from_bf2(word(xv[j], i));
-                    u64 y;
-                    if (OP == kOpLN) {
-                        y = f2_mul(f2_sub(xx, mean2), rstd2);
+            for (int j = 0; j < V; ++j) {
+                const int v = j * 32 + lane;
+                if (EXACT || v < seg_len) {
+                    uint4 s1, h, w = make_uint4(0u, 0u, 0u, 0u);
+                    if (kCached) {
+                        s1 = c_s1[s0 + v];
+                        h = c_sh[s0 + v];
+                        if (OP != kOpLN && has_w)
+                            w = c_w[s0 + v];
                     } else {
-                        y = f2_mul(xx, rstd2);
-                        if (has_w)
-                            y = f2_mul(y, f2_from_bf2(word(w, i)));
+                        s1 = bf2x4_add(ld_cached(scale + b * a.mod_bstride + s0 + v), kBf2One);
+                        h = ld_cached(shift + b * a.mod_bstride + s0 + v);
+                        if (OP != kOpLN && has_w)
+                            w = ld_cached(weight + s0 + v);
                     }
-                    const uint32_t yb = bf2_from_f2(y);
-                    const uint32_t s1 = bf2_add(word(s, i), kBf2One);
-                    word(o, i) = bf2_add(bf2_mul(yb, s1), word(h, i));
+                    st_stream(out + base + v,
+                              normalise_modulate<OP>(xv[j], mean2, rstd2, s1, h, w, has_w));
                 }
-                st_stream(out + base + v, o);
             }
         }
+        uses += k;
     }
     // nothing is left in flight on the normal path (every issued row was
     // waited for); after a timeout, give outstanding copies a bounded time
@@ -370,33 +444,59 @@ __global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads)
         drain_pause();
 }
 
-template <int OP, int V, int WPR>
-cudaError_t launch_cfg(const RowArgs& a, const DeviceInfo& dev, cudaStream_t stream)
+template <int OP, int V, int WPR, bool EXACT>
+cudaError_t launch_shape(const RowArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
     using Shape = RowShape<OP, V, WPR>;
-    auto kern = row_kernel<OP, V, WPR>;
+    auto kern = row_kernel<OP, V, WPR, EXACT>;
+    constexpr int kSmemMax = Shape::kRingBytes + Shape::kCacheBytes;
     static int blocks_per_sm[64] = {0};
     const int d = dev.device & 63;
     if (blocks_per_sm[d] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Shape::kSmem);
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
         if (e != cudaSuccess)
             return e;
         int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Shape::kThreads,
-                                                          Shape::kSmem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Shape::kThreads, kSmemMax);
         if (e != cudaSuccess)
             return e;
         blocks_per_sm[d] = n > 0 ? n : 1;
     }
     constexpr int kGroups = Shape::kWarps / WPR;
-    const int64_t want = (a.rows + kGroups - 1) / kGroups;
     const int64_t cap = static_cast<int64_t>(dev.sms) * blocks_per_sm[d];
-    const int grid = static_cast<int>(want < cap ? want : cap);
-    kern<<<grid, Shape::kThreads, Shape::kSmem, stream>>>(a);
+    const int64_t B = a.rows / a.S;
+    // split each batch into enough items to fill the GPU, each item at least
+    // one row per group when the rows allow it
+    int64_t per_batch = cap / (B > 0 ? B : 1);
+    const int64_t max_items = (a.S + kGroups - 1) / kGroups;
+    if (per_batch > max_items)
+        per_batch = max_items;
+    if (per_batch < 1)
+        per_batch = 1;
+    Items items;
+    items.per_batch = per_batch;
+    items.chunk = (a.S + per_batch - 1) / per_batch;
+    items.count = B * per_batch;
+    const int grid = static_cast<int>(items.count < cap ? items.count : cap);
+    const int smem = Shape::kRingBytes + (Shape::kCached ? Shape::kNmod * a.Dv * 16 : 0);
+    kern<<<grid, Shape::kThreads, smem, stream>>>(a, items);
     return cudaGetLastError();
 }
 
+// Rows up to 1024 values: one warp each.  Longer rows are split over two or
+// four warps (contiguous segments), which keeps registers and shared memory
+// per warp small enough for ~24 resident warps per SM.
+template <int OP, int V, int WPR>
+cudaError_t launch_cfg(const RowArgs& a, const DeviceInfo& dev, cudaStream_t stream)
+{
+    if (a.Dv == 32 * V * WPR)
+        return launch_shape<OP, V, WPR, true>(a, dev, stream);
+    return launch_shape<OP, V, WPR, false>(a, dev, stream);
+}
+
+// Rows of up to 4096 values: one warp each (V vectors per lane); longer rows
+// are split over two or four warps (contiguous segments).
 template <int OP>
 cudaError_t launch_op(const RowArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {

@@ -13,7 +13,9 @@
 //
 //   xb  = R(x + R(bias))              (aten add_ arithmetic, before the statistics)
 //   z   = (xb * rstd) * gamma         (fp32, unrounded)
-//   out = R(z * sigmoid(z))
+//   out = R(z * sigmoid(z))  (z / (1 + exp(-z)) with hardware exp2 / reciprocal
+//                             approximations; an accurate form where |z| may
+//                             exceed 64)
 #include "device_common.cuh"
 #include "launch.h"
 
@@ -42,14 +44,38 @@ struct WanShape {
     static constexpr int kSmem = kWarps * kStages * kTileVec * 16;
 };
 
-// SiLU(z) = z * sigmoid(z), sigmoid from e = exp(-|z|) in (0, 1] so nothing
-// overflows: sigmoid = 1 / (1 + e) for z >= 0 and e / (1 + e) below zero.
-__device__ __forceinline__ float silu(float z)
+// SiLU(z) = z * sigmoid(z) with sigmoid from e = exp(-|z|) in (0, 1], so
+// nothing overflows: 1 / (1 + e) for z >= 0 and e / (1 + e) below zero.
+// Accurate exp; used for pixels whose |z| may exceed kFastSiluLimit.
+__device__ __forceinline__ float silu_wide(float z)
 {
     const float e = expf(-fabsf(z));
     const float r = __fdividef(1.0f, __fadd_rn(1.0f, e));
     const float s = z >= 0.0f ? r : __fmul_rn(e, r);
     return __fmul_rn(z, s);
+}
+
+// Two SiLUs as z / (1 + 2^(-z * log2 e)) with the hardware exp2 and
+// reciprocal approximations (relative error ~2^-21 for |z| <= 64, far below
+// a bf16 rounding step).  For z > 87 the exponential underflows to 0 and
+// the result is z; below about -88 it would overflow, which the caller
+// excludes with a bound on |z|.
+constexpr float kFastSiluLimit = 64.0f;
+
+__device__ __forceinline__ u64 silu2_fast(u64 z)
+{
+    const u64 t = f2_mul(z, f2_splat(-1.4426950408889634f));
+    float t0, t1;
+    f2_unpack(t, t0, t1);
+    float e0, e1;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(t0));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(t1));
+    float d0, d1;
+    f2_unpack(f2_add(f2_pack(e0, e1), f2_splat(1.0f)), d0, d1);
+    float r0, r1;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(d0));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(d1));
+    return f2_mul(z, f2_pack(r0, r1));
 }
 
 template <int P, int V>
@@ -75,6 +101,7 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
     // this lane's channels: vectors sub + P * j
     uint32_t b16[V][4];
     u64 g2[V][4];
+    uint32_t gmax_bits = 0;
 #pragma unroll
     for (int j = 0; j < V; ++j) {
         const int c = sub + P * j;
@@ -96,8 +123,11 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
         for (int i = 0; i < 4; ++i) {
             g2[j][i] = f2_from_bf2(word(g, i));
             b16[j][i] = word(bb, i);
+            gmax_bits = bf2_absmax(gmax_bits, word(g, i));
         }
     }
+    // |gamma| of this lane's channels, for the per-pixel bound on |z|
+    const float gmax = __uint_as_float(absmax_bits(gmax_bits) << 16);
 
     uint4* wbuf = ring + warp * kStages * kTileVec;
     const uint32_t bar0 = smem_addr(&bars[warp][0]);
@@ -171,13 +201,19 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
         const uint32_t mm = absmax_bits(m);
         const uint32_t E = offset_exponent(mm);
 
+        u64 xf[V][4];
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                xf[j][i] = f2_from_bf2(word(xv[j], i));
         ExactSums<false> acc;
         acc.init(offset_k1<kL>(E), offset_k2<kL>(E));
 #pragma unroll
         for (int j = 0; j < V; ++j)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                acc.add(f2_from_bf2(word(xv[j], i)));
+                acc.add(xf[j][i]);
         float s1h, s1l, s2h, s2l;
         acc.lane_total(s1h, s1l, s2h, s2l);
         dd_allreduce<P>(s2h, s2l);
@@ -217,6 +253,12 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
             a.rstd_out[pix] = rstd;
 
         const u64 rstd2 = f2_splat(rstd);
+        // |z| <= max|xb| * rstd * max|gamma|: the fast SiLU is exact enough
+        // below the limit; any pixel of the warp above it (or NaN) sends the
+        // whole step through the accurate form
+        const float zbound =
+            __fmul_rn(__fmul_rn(__uint_as_float(mm << 16), rstd), gmax);
+        const bool wide = __any_sync(kFullMask, !(zbound <= kFastSiluLimit));
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int c = sub + P * j;
@@ -224,10 +266,14 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
                 uint4 o;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const u64 z = f2_mul(f2_mul(f2_from_bf2(word(xv[j], i)), rstd2), g2[j][i]);
-                    float z0, z1;
-                    f2_unpack(z, z0, z1);
-                    word(o, i) = pack_bf2(silu(z0), silu(z1));
+                    const u64 z = f2_mul(f2_mul(xf[j][i], rstd2), g2[j][i]);
+                    if (!wide) {
+                        word(o, i) = bf2_from_f2(silu2_fast(z));
+                    } else {
+                        float z0, z1;
+                        f2_unpack(z, z0, z1);
+                        word(o, i) = pack_bf2(silu_wide(z0), silu_wide(z1));
+                    }
                 }
                 st_stream(out + base + c, o);
             }

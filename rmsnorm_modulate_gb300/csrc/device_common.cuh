@@ -241,6 +241,16 @@ __device__ __forceinline__ void f2_unpack(u64 v, float& lo, float& hi)
 __device__ __forceinline__ u64 f2_splat(float v) { return f2_pack(v, v); }
 
 // The two bf16 of a word widened exactly to an fp32 pair.
+// First statement of every kernel (they are launched as programmatic
+// dependents): waits until the previous grid in the stream has completed and
+// its memory is visible, then lets the next grid's CTAs be scheduled as this
+// grid's CTAs retire.  No global memory is touched before it.
+__device__ __forceinline__ void grid_dependency_sync()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ u64 f2_from_bf2(uint32_t w)
 {
     return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));

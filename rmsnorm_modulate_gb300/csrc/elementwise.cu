@@ -66,6 +66,7 @@ template <int OP>
 __global__ void __launch_bounds__(kThreads)
     ew_kernel(const EwArgs a, uint32_t total, FastDiv fd_row, FastDiv fd_batch)
 {
+    grid_dependency_sync();
     const uint4* __restrict__ src = static_cast<const uint4*>(a.a);
     uint4* __restrict__ dst = static_cast<uint4*>(a.out);
     const uint32_t stride = gridDim.x * kThreads;
@@ -105,8 +106,7 @@ cudaError_t launch(const EwArgs& a, const DeviceInfo& dev, cudaStream_t stream)
     const int grid = static_cast<int>(want < cap ? want : cap);
     const FastDiv fd_row = FastDiv::make(static_cast<uint32_t>(a.Dv));
     const FastDiv fd_batch = FastDiv::make(static_cast<uint32_t>(a.S > 0 ? a.S : 1));
-    ew_kernel<OP><<<grid, kThreads, 0, stream>>>(a, total, fd_row, fd_batch);
-    return cudaGetLastError();
+    return launch_dependent(ew_kernel<OP>, grid, kThreads, 0, stream, a, total, fd_row, fd_batch);
 }
 
 }  // namespace

@@ -39,6 +39,28 @@ struct FastDiv {
 
 enum RowOp : int { kOpLN = 0, kOpRMS = 1, kOpGated = 2 };
 
+// Every kernel is launched with programmatic stream serialisation: its CTAs
+// may be scheduled while the previous grid in the stream is draining, and the
+// kernel's first statement (griddepcontrol.wait) holds them until that grid
+// has completed and its writes are visible, so ordering is unchanged and only
+// the launch gap is hidden.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), int grid, int block, int smem,
+                             cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(block));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 struct RowArgs {
     const void* x;         // LN / RMS input rows
     const void* residual;  // gated

@@ -34,6 +34,7 @@ constexpr int kL = 5;                             // 32 values per lane = 2^5
 
 __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blocks_q)
 {
+    grid_dependency_sync();
     extern __shared__ __align__(128) uint4 ring[];
     __shared__ __align__(8) unsigned long long bars[kWarps][kStages];
 
@@ -239,8 +240,7 @@ cudaError_t launch_qk_kernel(const QkArgs& a, const DeviceInfo& dev, cudaStream_
         bk = cap - bq;
     }
     const int grid = static_cast<int>(bq + bk);
-    qk_kernel<<<grid, kThreads, kSmem, stream>>>(a, static_cast<int>(bq));
-    return cudaGetLastError();
+    return launch_dependent(qk_kernel, grid, kThreads, kSmem, stream, a, static_cast<int>(bq));
 }
 
 cudaError_t qk_kernel_error(unsigned* bits, bool clear)

@@ -229,6 +229,7 @@ template <int OP, int V, int WPR, bool EXACT>
 __global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads, RowShape<OP, V, WPR>::kBlocks)
     row_kernel(const RowArgs a, const Items items)
 {
+    grid_dependency_sync();
     using Shape = RowShape<OP, V, WPR>;
     constexpr int kWarps = Shape::kWarps;
     constexpr int kGroups = kWarps / WPR;
@@ -480,8 +481,7 @@ cudaError_t launch_shape(const RowArgs& a, const DeviceInfo& dev, cudaStream_t s
     items.count = B * per_batch;
     const int grid = static_cast<int>(items.count < cap ? items.count : cap);
     const int smem = Shape::kRingBytes + (Shape::kCached ? Shape::kNmod * a.Dv * 16 : 0);
-    kern<<<grid, Shape::kThreads, smem, stream>>>(a, items);
-    return cudaGetLastError();
+    return launch_dependent(kern, grid, Shape::kThreads, smem, stream, a, items);
 }
 
 // Rows up to 1024 values: one warp each.  Longer rows are split over two or

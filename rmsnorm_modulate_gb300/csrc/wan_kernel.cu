@@ -28,6 +28,7 @@ __device__ unsigned int g_error;
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kStages = 6;
+constexpr int kMaxVecPerLane = 4;
 
 template <int N>
 struct Log2Ceil {
@@ -78,13 +79,15 @@ __device__ __forceinline__ u64 silu2_fast(u64 z)
     return f2_mul(z, f2_pack(r0, r1));
 }
 
-template <int P, int V>
+// EXACT: C == 8 * P * V, so no channel vector needs a bounds check.
+template <int P, int V, bool EXACT>
 __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
 {
     constexpr int kL = Log2Ceil<8 * V>::value;
     constexpr int kPix = 32 / P;  // pixels per warp step
     constexpr int kTileVec = WanShape<V>::kTileVec;
 
+    grid_dependency_sync();
     extern __shared__ __align__(128) uint4 ring[];
     __shared__ __align__(8) unsigned long long bars[kWarps][kStages];
 
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int c = sub + P * j;
-            if (valid && c < Cv) {
+            if (valid && (EXACT || c < Cv)) {
                 uint4 v = tile[c];
                 if (has_bias) {
 #pragma unroll
@@ -192,28 +195,16 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
         __syncwarp();
         issue(k + kStages);
 
-        uint32_t m = 0;
-#pragma unroll
-        for (int j = 0; j < V; ++j)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                m = bf2_absmax(m, word(xv[j], i));
-        const uint32_t mm = absmax_bits(m);
+        const uint32_t mm = tree_absmax<V>(xv);
         const uint32_t E = offset_exponent(mm);
 
-        u64 xf[V][4];
-#pragma unroll
-        for (int j = 0; j < V; ++j)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                xf[j][i] = f2_from_bf2(word(xv[j], i));
         ExactSums<false> acc;
         acc.init(offset_k1<kL>(E), offset_k2<kL>(E));
 #pragma unroll
         for (int j = 0; j < V; ++j)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                acc.add(xf[j][i]);
+                acc.add(f2_from_bf2(word(xv[j], i)));
         float s1h, s1l, s2h, s2l;
         acc.lane_total(s1h, s1l, s2h, s2l);
         dd_allreduce<P>(s2h, s2l);
@@ -262,11 +253,12 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int c = sub + P * j;
-            if (valid && c < Cv) {
+            if (valid && (EXACT || c < Cv)) {
                 uint4 o;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const u64 z = f2_mul(f2_mul(xf[j][i], rstd2), g2[j][i]);
+                    const u64 z =
+                        f2_mul(f2_mul(f2_from_bf2(word(xv[j], i)), rstd2), g2[j][i]);
                     if (!wide) {
                         word(o, i) = bf2_from_f2(silu2_fast(z));
                     } else {
@@ -283,10 +275,10 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
         drain_pause();
 }
 
-template <int P, int V>
-cudaError_t launch_cfg(const WanArgs& a, const DeviceInfo& dev, cudaStream_t stream)
+template <int P, int V, bool EXACT>
+cudaError_t launch_shape(const WanArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
-    auto kern = wan_kernel<P, V>;
+    auto kern = wan_kernel<P, V, EXACT>;
     constexpr int kSmem = WanShape<V>::kSmem;
     static int blocks_per_sm[64] = {0};
     const int d = dev.device & 63;
@@ -305,24 +297,28 @@ cudaError_t launch_cfg(const WanArgs& a, const DeviceInfo& dev, cudaStream_t str
     const int64_t want = (a.pixels + kPixPerBlock - 1) / kPixPerBlock;
     const int64_t cap = static_cast<int64_t>(dev.sms) * blocks_per_sm[d];
     const int grid = static_cast<int>(want < cap ? want : cap);
-    kern<<<grid, kThreads, kSmem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(kern, grid, kThreads, kSmem, stream, a);
+}
+
+template <int P, int V>
+cudaError_t launch_cfg(const WanArgs& a, const DeviceInfo& dev, cudaStream_t stream)
+{
+    if (a.Cv == P * V)
+        return launch_shape<P, V, true>(a, dev, stream);
+    return launch_shape<P, V, false>(a, dev, stream);
 }
 
 template <int P>
 cudaError_t launch_p(const WanArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
     const int V = (a.Cv + P - 1) / P;
-    switch (V) {
-    case 1:
+    if (V <= 1)
         return launch_cfg<P, 1>(a, dev, stream);
-    case 2:
+    if (V <= 2)
         return launch_cfg<P, 2>(a, dev, stream);
-    case 3:
+    if (V <= 3)
         return launch_cfg<P, 3>(a, dev, stream);
-    default:
-        return launch_cfg<P, 4>(a, dev, stream);
-    }
+    return launch_cfg<P, 4>(a, dev, stream);
 }
 
 }  // namespace
@@ -332,7 +328,7 @@ cudaError_t launch_p(const WanArgs& a, const DeviceInfo& dev, cudaStream_t strea
 // C = 384 -> 16 x 3, C = 1024 -> 32 x 4.
 cudaError_t launch_wan_kernel(const WanArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
-    const int need = (a.Cv + 3) / 4;
+    const int need = (a.Cv + kMaxVecPerLane - 1) / kMaxVecPerLane;
     if (need <= 1)
         return launch_p<1>(a, dev, stream);
     if (need <= 2)

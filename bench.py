@@ -193,18 +193,33 @@ def run_reference(args, rank, world):
 # the CUDA arm
 # --------------------------------------------------------------------------
 
-def traffic_record(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (the summary records the source digest)."""
+# sources each kernel is built from (a change to any of them makes a stored
+# DRAM-traffic figure stale)
+KERNEL_SOURCES = {
+    "row_kernel": ("row_kernels.cu", "device_common.cuh", "launch.h"),
+    "qk_kernel": ("qk_kernel.cu", "device_common.cuh", "launch.h"),
+    "wan_kernel": ("wan_kernel.cu", "device_common.cuh", "launch.h"),
+}
+
+
+def source_digest(kernel: str) -> str:
     import hashlib
 
-    path = os.path.join(ROOT, "profiles", "traffic.md")
     src = os.path.join(ROOT, "rmsnorm_modulate_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(src)):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(src, f), "rb") as fh:
+            h.update(f.encode())
             h.update(fh.read())
-    digest = h.hexdigest()[:16]
+    return h.hexdigest()[:16]
+
+
+def traffic_record(kernel: str, workload: str):
+    """DRAM bytes (read + write) per launch from the committed ncu summary
+    table, if it was taken on the kernel's current source (each row records
+    the digest of the sources the kernel is built from)."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    digest = source_digest(kernel)
     try:
         with open(path) as fh:
             for line in fh:
@@ -396,7 +411,10 @@ def main():
         "ln_modulate_1x4608x3072": {"us": 1e3 * t1, "gbs": b1 / (t1 * 1e-3) / 1e9},
         "ln_modulate_2x4608x3072": {"us": 1e3 * t2, "gbs": b2 / (t2 * 1e-3) / 1e9},
     }
-    traffic = traffic_record("row_kernel<0,12,1>", "ln_modulate_flux_2x4608x3072")
+    # DRAM bytes of the average launch (the step is one launch of each shape)
+    t_b1 = traffic_record("row_kernel", "ln_modulate_flux_1x4608x3072")
+    t_b2 = traffic_record("row_kernel", "ln_modulate_flux_2x4608x3072")
+    traffic = (t_b1 + t_b2) / 2 if t_b1 is not None and t_b2 is not None else None
 
     # ---- end to end through the C ABI from pinned host buffers -----------
     e2e = None
@@ -471,7 +489,8 @@ def main():
         "pct_of_nominal_8tbs": 100.0 * value / world / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "row_kernel<0,12,1> (ln_modulate, D=3072)",
+                     "kernel": "row_kernel<LN, V=12, 1 warp/row> (ln_modulate, D=3072)",
+                     "traffic_per": "average launch of the step (B=1 and B=2 shapes)",
                      "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                      "algorithmic_bytes_per_launch": {"B1": b1, "B2": b2}},
         "per_launch": per_launch,

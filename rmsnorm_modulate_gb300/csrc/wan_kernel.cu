@@ -7,9 +7,10 @@
 // byte range.  P lanes share a pixel (V 16-byte vectors each, P * V * 8 >= C)
 // and a warp covers 32 / P consecutive pixels per step; that tile is one
 // contiguous span of at most 32 * V vectors, brought into shared memory by a
-// 1-D bulk copy (TMA) into a six-stage ring per warp.  A lane's channels
-// never change, so its bias (rounded to bf16 once) and gamma (widened to
-// fp32 once) stay in registers for the whole kernel.
+// 1-D bulk copy (TMA) into a ring of kStages tiles per warp.  Gamma and the
+// bias (rounded to bf16 once) are staged in shared memory per CTA, so a lane
+// carries only its pixel's values in registers and V can be large enough to
+// amortise the per-pixel reduction, rstd and bound checks over many values.
 //
 //   xb  = R(x + R(bias))              (aten add_ arithmetic, before the statistics)
 //   z   = (xb * rstd) * gamma         (fp32, unrounded)
@@ -27,8 +28,10 @@ __device__ unsigned int g_error;
 
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kStages = 6;
-constexpr int kMaxVecPerLane = 4;
+// vectors per lane the lane split aims for (P = smallest power of two with
+// P * kVecTarget >= C / 8)
+constexpr int kVecTarget = 6;
+constexpr int kMaxCv = 1024 / 8;  // C <= 1024
 
 template <int N>
 struct Log2Ceil {
@@ -41,8 +44,9 @@ struct Log2Ceil<1> {
 
 template <int V>
 struct WanShape {
-    static constexpr int kTileVec = 32 * V;  // buffer capacity in 16-byte vectors
-    static constexpr int kSmem = kWarps * kStages * kTileVec * 16;
+    static constexpr int kTileVec = 32 * V;  // tile capacity in 16-byte vectors
+    static constexpr int kStages = V >= 6 ? 4 : 6;
+    static constexpr int kRingBytes = kWarps * kStages * kTileVec * 16;
 };
 
 // SiLU(z) = z * sigmoid(z) with sigmoid from e = exp(-|z|) in (0, 1], so
@@ -81,15 +85,17 @@ __device__ __forceinline__ u64 silu2_fast(u64 z)
 
 // EXACT: C == 8 * P * V, so no channel vector needs a bounds check.
 template <int P, int V, bool EXACT>
-__global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
+__global__ void __launch_bounds__(kThreads, 2) wan_kernel(const WanArgs a)
 {
+    grid_dependency_sync();
     constexpr int kL = Log2Ceil<8 * V>::value;
     constexpr int kPix = 32 / P;  // pixels per warp step
     constexpr int kTileVec = WanShape<V>::kTileVec;
+    constexpr int kStages = WanShape<V>::kStages;
 
-    grid_dependency_sync();
     extern __shared__ __align__(128) uint4 ring[];
     __shared__ __align__(8) unsigned long long bars[kWarps][kStages];
+    __shared__ uint32_t s_gmax;
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -100,37 +106,8 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
     const uint4* __restrict__ x = static_cast<const uint4*>(a.x);
     uint4* __restrict__ out = static_cast<uint4*>(a.out);
     const bool has_bias = a.bias != nullptr;
-
-    // this lane's channels: vectors sub + P * j
-    uint32_t b16[V][4];
-    u64 g2[V][4];
-    uint32_t gmax_bits = 0;
-#pragma unroll
-    for (int j = 0; j < V; ++j) {
-        const int c = sub + P * j;
-        uint4 g = make_uint4(0u, 0u, 0u, 0u), bb = make_uint4(0u, 0u, 0u, 0u);
-        if (c < Cv) {
-            g = ld_cached(static_cast<const uint4*>(a.gamma) + c);
-            if (has_bias) {
-                if (a.bias_is_fp32) {
-                    const float4* bf = static_cast<const float4*>(a.bias) + 2 * c;
-                    const float4 lo = ld_cached_f4(bf), hi = ld_cached_f4(bf + 1);
-                    bb = make_uint4(pack_bf2(lo.x, lo.y), pack_bf2(lo.z, lo.w),
-                                    pack_bf2(hi.x, hi.y), pack_bf2(hi.z, hi.w));
-                } else {
-                    bb = ld_cached(static_cast<const uint4*>(a.bias) + c);
-                }
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            g2[j][i] = f2_from_bf2(word(g, i));
-            b16[j][i] = word(bb, i);
-            gmax_bits = bf2_absmax(gmax_bits, word(g, i));
-        }
-    }
-    // |gamma| of this lane's channels, for the per-pixel bound on |z|
-    const float gmax = __uint_as_float(absmax_bits(gmax_bits) << 16);
+    uint4* c_gamma = ring + WanShape<V>::kRingBytes / 16;
+    uint4* c_bias = c_gamma + Cv;
 
     uint4* wbuf = ring + warp * kStages * kTileVec;
     const uint32_t bar0 = smem_addr(&bars[warp][0]);
@@ -140,6 +117,8 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
             mbar_init(bar0 + 8u * s, 1u);
         mbar_init_fence();
     }
+    if (threadIdx.x == 0)
+        s_gmax = 0u;
     __syncwarp();
 
     const int64_t first = static_cast<int64_t>(blockIdx.x) * kWarps + warp;  // tile index
@@ -160,6 +139,33 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
 #pragma unroll
     for (int k = 0; k < kStages; ++k)
         issue(k);
+
+    // gamma and R(bias) for every channel, and max |gamma| (the bound on |z|
+    // below uses it), while the first tiles are in flight
+    __syncthreads();
+    {
+        uint32_t gm = 0;
+        for (int c = threadIdx.x; c < Cv; c += kThreads) {
+            const uint4 g = ld_cached(static_cast<const uint4*>(a.gamma) + c);
+            uint4 bb = make_uint4(0u, 0u, 0u, 0u);
+            if (has_bias) {
+                if (a.bias_is_fp32) {
+                    const float4* bf = static_cast<const float4*>(a.bias) + 2 * c;
+                    const float4 lo = ld_cached_f4(bf), hi = ld_cached_f4(bf + 1);
+                    bb = make_uint4(pack_bf2(lo.x, lo.y), pack_bf2(lo.z, lo.w),
+                                    pack_bf2(hi.x, hi.y), pack_bf2(hi.z, hi.w));
+                } else {
+                    bb = ld_cached(static_cast<const uint4*>(a.bias) + c);
+                }
+            }
+            c_gamma[c] = g;
+            c_bias[c] = bb;
+            gm = bf2_absmax(bf2_absmax(gm, bf2_absmax(g.x, g.y)), bf2_absmax(g.z, g.w));
+        }
+        atomicMax(&s_gmax, absmax_bits(gm));
+    }
+    __syncthreads();
+    const float gmax = __uint_as_float(s_gmax << 16);
 
     bool broken = false;
     for (int64_t k = 0; (first + k * step) * kPix < a.pixels; ++k) {
@@ -183,9 +189,10 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
             if (valid && (EXACT || c < Cv)) {
                 uint4 v = tile[c];
                 if (has_bias) {
+                    const uint4 bb = c_bias[c];
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        word(v, i) = bf2_add(word(v, i), b16[j][i]);
+                        word(v, i) = bf2_add(word(v, i), word(bb, i));
                 }
                 xv[j] = v;
             } else {
@@ -254,11 +261,12 @@ __global__ void __launch_bounds__(kThreads) wan_kernel(const WanArgs a)
         for (int j = 0; j < V; ++j) {
             const int c = sub + P * j;
             if (valid && (EXACT || c < Cv)) {
+                const uint4 g = c_gamma[c];
                 uint4 o;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const u64 z =
-                        f2_mul(f2_mul(f2_from_bf2(word(xv[j], i)), rstd2), g2[j][i]);
+                    const u64 z = f2_mul(f2_mul(f2_from_bf2(word(xv[j], i)), rstd2),
+                                         f2_from_bf2(word(g, i)));
                     if (!wide) {
                         word(o, i) = bf2_from_f2(silu2_fast(z));
                     } else {
@@ -279,16 +287,17 @@ template <int P, int V, bool EXACT>
 cudaError_t launch_shape(const WanArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
     auto kern = wan_kernel<P, V, EXACT>;
-    constexpr int kSmem = WanShape<V>::kSmem;
+    constexpr int kSmemMax = WanShape<V>::kRingBytes + 2 * kMaxCv * 16;
     static int blocks_per_sm[64] = {0};
     const int d = dev.device & 63;
     if (blocks_per_sm[d] == 0) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmem);
+                                             kSmemMax);
         if (e != cudaSuccess)
             return e;
         int nb = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads, kSmem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads,
+                                                          WanShape<V>::kRingBytes + 2 * a.Cv * 16);
         if (e != cudaSuccess)
             return e;
         blocks_per_sm[d] = nb > 0 ? nb : 1;
@@ -297,7 +306,8 @@ cudaError_t launch_shape(const WanArgs& a, const DeviceInfo& dev, cudaStream_t s
     const int64_t want = (a.pixels + kPixPerBlock - 1) / kPixPerBlock;
     const int64_t cap = static_cast<int64_t>(dev.sms) * blocks_per_sm[d];
     const int grid = static_cast<int>(want < cap ? want : cap);
-    return launch_dependent(kern, grid, kThreads, kSmem, stream, a);
+    const int smem = WanShape<V>::kRingBytes + 2 * a.Cv * 16;
+    return launch_dependent(kern, grid, kThreads, smem, stream, a);
 }
 
 template <int P, int V>
@@ -318,17 +328,16 @@ cudaError_t launch_p(const WanArgs& a, const DeviceInfo& dev, cudaStream_t strea
         return launch_cfg<P, 2>(a, dev, stream);
     if (V <= 3)
         return launch_cfg<P, 3>(a, dev, stream);
-    return launch_cfg<P, 4>(a, dev, stream);
+    if (V <= 4)
+        return launch_cfg<P, 4>(a, dev, stream);
+    return launch_cfg<P, kVecTarget>(a, dev, stream);
 }
 
 }  // namespace
 
-// P = the smallest power of two with P * 4 >= C / 8 (at most 32), so a lane
-// holds at most four vectors: C = 96 -> 4 lanes x 3, C = 192 -> 8 x 3,
-// C = 384 -> 16 x 3, C = 1024 -> 32 x 4.
 cudaError_t launch_wan_kernel(const WanArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
-    const int need = (a.Cv + kMaxVecPerLane - 1) / kMaxVecPerLane;
+    const int need = (a.Cv + kVecTarget - 1) / kVecTarget;
     if (need <= 1)
         return launch_p<1>(a, dev, stream);
     if (need <= 2)

@@ -2,15 +2,17 @@
 // rows in one launch (sglang #34008 GLM-Image, §Motivation qk-norm bullet and
 // §What "rounding-faithful" means here, qk bullet).
 //
-// A 128-element head row is 256 bytes.  Four lanes own one row (32 values
-// each, as four 16-byte vectors), so one warp covers a tile of eight
-// consecutive rows (2 KB) per step and every lane is busy -- the eager
-// kernel spends a 128-thread block per row with three of its four warps
-// idle.  Tiles reach shared memory by 1-D bulk copies (TMA) into a
-// four-stage ring per warp, so three tiles are in flight while one is
-// computed.  Blocks are split between the q rows and the k rows in
-// proportion, so a lane's weight and bias (32 columns, kept as fp32 pairs
-// in registers) are loaded once per kernel.
+// A 128-element head row is 256 bytes (16 vectors of eight bf16).  P lanes
+// own one row (16 / P vectors each), so a warp covers a tile of 32 / P
+// consecutive rows per step and every lane is busy -- the eager kernel
+// spends a 128-thread block per row with three of its four warps idle.
+// Tiles reach shared memory by 1-D bulk copies (TMA) into a ring per warp,
+// so the next tiles are in flight while one is computed.  Blocks are split
+// between the q rows and the k rows in proportion; a block stages its
+// weight and bias once, widened to fp32, in shared memory.  A lane visits
+// its vectors in an order rotated by its row inside the tile, which keeps
+// the row reads (256-byte stride) and the weight reads free of bank
+// conflicts.
 //
 //   z = R(((x - mean) * rstd) * w + b)   -- fp32, one final rounding
 #include "device_common.cuh"
@@ -24,19 +26,23 @@ __device__ unsigned int g_error;
 
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kLanesPerRow = 4;
-constexpr int kVecPerLane = 4;                    // 4 x 8 = 32 values per lane
+constexpr int kRowVec = 16;                       // 16-byte vectors per row
+constexpr int kLanesPerRow = 2;                   // P
+constexpr int kVecPerLane = kRowVec / kLanesPerRow;
 constexpr int kTileRows = 32 / kLanesPerRow;      // rows per warp step
-constexpr int kTileVec = kTileRows * 16;          // 16-byte vectors per tile
-constexpr int kStages = 4;
+constexpr int kTileVec = kTileRows * kRowVec;     // 16-byte vectors per tile
+constexpr int kStages = 3;
 constexpr int kSmem = kWarps * kStages * kTileVec * 16;
-constexpr int kL = 5;                             // 32 values per lane = 2^5
+constexpr int kL = 6;                             // 8 * kVecPerLane = 2^kL values per lane
+static_assert((8 << kL) == 8 * 8 * kVecPerLane, "kL must be log2 of the values per lane");
 
 __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blocks_q)
 {
     grid_dependency_sync();
     extern __shared__ __align__(128) uint4 ring[];
     __shared__ __align__(8) unsigned long long bars[kWarps][kStages];
+    // weight and bias of this block's tensor, fp32, as [vector][half] float4
+    __shared__ __align__(16) float4 s_w[2][kRowVec], s_b[2][kRowVec];
 
     const bool is_q = static_cast<int>(blockIdx.x) < blocks_q;
     const int64_t rows = is_q ? a.rows_q : a.rows_k;
@@ -50,21 +56,9 @@ __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blo
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int sub = lane & (kLanesPerRow - 1);   // position inside the row
-    const int rsub = lane / kLanesPerRow;        // row inside the tile
-
-    // this lane's columns: vectors sub, sub + 4, sub + 8, sub + 12
-    u64 w2[kVecPerLane][4], b2[kVecPerLane][4];
-#pragma unroll
-    for (int j = 0; j < kVecPerLane; ++j) {
-        uint4 w = ld_cached(wv + sub + kLanesPerRow * j);
-        uint4 b = ld_cached(bv + sub + kLanesPerRow * j);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            w2[j][i] = f2_from_bf2(word(w, i));
-            b2[j][i] = f2_from_bf2(word(b, i));
-        }
-    }
+    const int sub = lane % kLanesPerRow;   // position inside the row
+    const int rsub = lane / kLanesPerRow;  // row inside the tile
+    const int rot = rsub % kVecPerLane;
 
     uint4* wbuf = ring + warp * kStages * kTileVec;
     const uint32_t bar0 = smem_addr(&bars[warp][0]);
@@ -88,11 +82,26 @@ __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blo
         const uint32_t bar = bar0 + 8u * st;
         fence_proxy_async();
         mbar_expect_tx(bar, bytes);
-        bulk_g2s(smem_addr(wbuf + st * kTileVec), src + row0 * 16, bytes, bar);
+        bulk_g2s(smem_addr(wbuf + st * kTileVec), src + row0 * kRowVec, bytes, bar);
     };
 #pragma unroll
     for (int k = 0; k < kStages; ++k)
         issue(k);
+
+    if (threadIdx.x < 2 * kRowVec) {
+        const int c = threadIdx.x >> 1, h = threadIdx.x & 1;
+        const uint4 w = ld_cached(wv + c), b = ld_cached(bv + c);
+        const uint32_t w0 = h ? w.z : w.x, w1 = h ? w.w : w.y;
+        const uint32_t b0 = h ? b.z : b.x, b1 = h ? b.w : b.y;
+        float l0, h0, l1, h1;
+        f2_unpack(f2_from_bf2(w0), l0, h0);
+        f2_unpack(f2_from_bf2(w1), l1, h1);
+        s_w[h][c] = make_float4(l0, h0, l1, h1);
+        f2_unpack(f2_from_bf2(b0), l0, h0);
+        f2_unpack(f2_from_bf2(b1), l1, h1);
+        s_b[h][c] = make_float4(l0, h0, l1, h1);
+    }
+    __syncthreads();
 
     const float n = 128.0f, inv_n = 1.0f / 128.0f;
     bool broken = false;
@@ -107,24 +116,20 @@ __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blo
         }
         const int64_t row = row0 + rsub;
         const bool valid = row < rows;
-        const int64_t base = row * 16;
+        const int64_t base = row * kRowVec;
 
-        const uint4* tile = wbuf + st * kTileVec + rsub * 16;
+        // vector j of this lane is c(j) = sub + P * ((j + rot) mod V)
+        const uint4* tile = wbuf + st * kTileVec + rsub * kRowVec;
         uint4 xv[kVecPerLane];
 #pragma unroll
-        for (int j = 0; j < kVecPerLane; ++j)
-            xv[j] = valid ? tile[sub + kLanesPerRow * j] : make_uint4(0u, 0u, 0u, 0u);
+        for (int j = 0; j < kVecPerLane; ++j) {
+            const int jj = (j + rot) % kVecPerLane;
+            xv[j] = valid ? tile[sub + kLanesPerRow * jj] : make_uint4(0u, 0u, 0u, 0u);
+        }
         __syncwarp();
         issue(k + kStages);
 
-        uint32_t m = 0;
-#pragma unroll
-        for (int j = 0; j < kVecPerLane; ++j)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                m = bf2_absmax(m, word(xv[j], i));
-        const uint32_t mm = absmax_bits(m);
-
+        const uint32_t mm = tree_absmax<kVecPerLane>(xv);
         ExactSums<true> acc;
         const uint32_t E = offset_exponent(mm);
         acc.init(offset_k1<kL>(E), offset_k2<kL>(E));
@@ -137,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blo
         acc.lane_total(s1h, s1l, s2h, s2l);
         dd2_allreduce<kLanesPerRow>(s1h, s1l, s2h, s2l);
 
-        // row class over its four lanes
+        // row class over its lanes
         uint32_t cls = allreduce_max<kLanesPerRow>(static_cast<uint32_t>(magnitude_class(mm)));
         uint32_t emax = allreduce_max<kLanesPerRow>(mm == 0 ? 0u : (mm >> 7));
 
@@ -189,15 +194,21 @@ __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blo
             const u64 mean2 = f2_splat(mean), rstd2 = f2_splat(rstd);
 #pragma unroll
             for (int j = 0; j < kVecPerLane; ++j) {
+                const int c = sub + kLanesPerRow * ((j + rot) % kVecPerLane);
+                const float4 w_lo = s_w[0][c], w_hi = s_w[1][c];
+                const float4 b_lo = s_b[0][c], b_hi = s_b[1][c];
+                const u64 w2[4] = {f2_pack(w_lo.x, w_lo.y), f2_pack(w_lo.z, w_lo.w),
+                                   f2_pack(w_hi.x, w_hi.y), f2_pack(w_hi.z, w_hi.w)};
+                const u64 b2[4] = {f2_pack(b_lo.x, b_lo.y), f2_pack(b_lo.z, b_lo.w),
+                                   f2_pack(b_hi.x, b_hi.y), f2_pack(b_hi.z, b_hi.w)};
                 uint4 o;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const u64 xx = f2_from_bf2(word(xv[j], i));
-                    const u64 z = f2_mul_then_add(f2_mul(f2_sub(xx, mean2), rstd2), w2[j][i],
-                                                  b2[j][i]);
+                    const u64 z = f2_mul_then_add(f2_mul(f2_sub(xx, mean2), rstd2), w2[i], b2[i]);
                     word(o, i) = bf2_from_f2(z);
                 }
-                st_stream(dst + base + sub + kLanesPerRow * j, o);
+                st_stream(dst + base + c, o);
             }
         }
     }

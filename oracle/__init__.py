@@ -20,6 +20,9 @@ Parity status per function (what pins it; see ``tests/test_oracle_*.py``):
 * ``ln_modulate``, ``rmsnorm_modulate``, ``gated_rmsnorm_modulate``,
   ``qk_layernorm``, ``rmsnorm_silu_cl``: fp64 brute force on small rows,
   closed forms, the bias-fold identity, permutation equivariance.
+* ``ln_modulate_folded``: fp64 brute force, torch layer_norm in fp64 with the
+  folded weight and bias, closed forms (zero modulation = LayerNorm, weight 2
+  doubles it, constant rows give the shift), the bound to the lossless chain.
 """
 from __future__ import annotations
 
@@ -75,6 +78,7 @@ def _load():
             lib.oracle_ln_normalize.argtypes = [P, P, I, I, F, P, P]
             lib.oracle_rms_normalize.argtypes = [P, P, P, I, I, F, P]
             lib.oracle_ln_modulate.argtypes = [P, P, P, P, I, I, I, I, F, P, P]
+            lib.oracle_ln_modulate_folded.argtypes = [P, P, P, P, I, I, I, I, F, P, P]
             lib.oracle_rmsnorm_modulate.argtypes = [P, P, P, P, P, I, I, I, I, F, P]
             lib.oracle_gated_rmsnorm_modulate.argtypes = [P, P, P, I, P, P, P, I, P, P, I, I,
                                                           I, F, P]
@@ -83,7 +87,8 @@ def _load():
             for name in ("oracle_round_bf16_array", "oracle_round_bf16_sweep", "oracle_modulate",
                          "oracle_residual_gate_add", "oracle_conv_bias_epilogue",
                          "oracle_row_stats", "oracle_ln_normalize", "oracle_rms_normalize",
-                         "oracle_ln_modulate", "oracle_rmsnorm_modulate",
+                         "oracle_ln_modulate", "oracle_ln_modulate_folded",
+                         "oracle_rmsnorm_modulate",
                          "oracle_gated_rmsnorm_modulate", "oracle_qk_layernorm",
                          "oracle_rmsnorm_silu_cl"):
                 getattr(lib, name).restype = None
@@ -228,6 +233,20 @@ def ln_modulate(x, scale, shift, eps=1e-6):
     rstd = np.empty(B * S, np.float32)
     _load().oracle_ln_modulate(_p(x), _p(sc), _p(sh), _p(out), B, S, D, bs, eps, _p(mean),
                                _p(rstd))
+    return out, mean, rstd
+
+
+def ln_modulate_folded(x, scale, shift, eps=1e-6):
+    """Single-rounding tier: x [B, S, D] -> (out, mean [B*S], rstd [B*S])."""
+    x = _u16(x)
+    B, S, D = x.shape
+    sc, bs = _mod_rows(scale, B, D)
+    sh, _ = _mod_rows(shift, B, D)
+    out = np.empty_like(x)
+    mean = np.empty(B * S, np.float32)
+    rstd = np.empty(B * S, np.float32)
+    _load().oracle_ln_modulate_folded(_p(x), _p(sc), _p(sh), _p(out), B, S, D, bs, eps,
+                                      _p(mean), _p(rstd))
     return out, mean, rstd
 
 

@@ -338,6 +338,43 @@ ORACLE_API void oracle_ln_modulate(const bf16_t* x, const bf16_t* scale, const b
     oracle_modulate(out, scale, shift, out, B, S, D, mod_bstride);
 }
 
+/* Single-rounding tier of LN + modulate ([FLUX] §Modifications commit 3,
+ * quality="high"): the modulate folds into the LayerNorm's elementwise
+ * affine, layer_norm(x, weight = R(1 + scale), bias = shift).  Only the
+ * [1, D] row 1 + scale keeps its eager rounding; the normalised value is not
+ * rounded before the affine, which runs in fp32 (a multiply, then an add, no
+ * FMA), and the result is rounded once:
+ *   w = R(1 + f(scale_b)),  out = R(((f(x) - mean) * rstd) * f(w) + f(shift_b)).
+ * Rows of batch b use scale_b = scale + b * mod_bstride, as ln_modulate. */
+ORACLE_API void oracle_ln_modulate_folded(const bf16_t* x, const bf16_t* scale,
+                                          const bf16_t* shift, bf16_t* out, int64_t B,
+                                          int64_t S, int64_t D, int64_t mod_bstride, float eps,
+                                          float* mean_out, float* rstd_out)
+{
+    for (int64_t b = 0; b < B; ++b) {
+        const bf16_t* sc = scale + b * mod_bstride;
+        const bf16_t* sh = shift + b * mod_bstride;
+        for (int64_t s = 0; s < S; ++s) {
+            const int64_t r = b * S + s;
+            const bf16_t* xr = x + r * D;
+            float mean, var;
+            ln_stats(xr, D, &mean, &var);
+            float rstd = rstd_of(var, eps);
+            for (int64_t d = 0; d < D; ++d) {
+                float w = widen(round_bf16(1.0f + widen(sc[d])));
+                float centred = widen(xr[d]) - mean;
+                float normed = centred * rstd;
+                float scaled = normed * w;
+                out[r * D + d] = round_bf16(scaled + widen(sh[d]));
+            }
+            if (mean_out)
+                mean_out[r] = mean;
+            if (rstd_out)
+                rstd_out[r] = rstd;
+        }
+    }
+}
+
 /* RMSNorm (optional weight) + modulate over x [B, S, D] ([ERNIE] first site). */
 ORACLE_API void oracle_rmsnorm_modulate(const bf16_t* x, const bf16_t* weight,
                                         const bf16_t* scale, const bf16_t* shift, bf16_t* out,

@@ -41,6 +41,13 @@ MUTATIONS = [
      "const bf16_t* g = gate;"),
     ("mean_square_not_squared", "csum_add(&s, v * v);", "csum_add(&s, v * fabs(v));"),
     ("mean_off_by_one_row", "ln_stats(xr, D, &mean, &var);", "ln_stats(xr, D - 1, &mean, &var);"),
+    ("folded_weight_not_rounded", "float w = widen(round_bf16(1.0f + widen(sc[d])));",
+     "float w = 1.0f + widen(sc[d]);"),
+    ("folded_one_minus_scale", "round_bf16(1.0f + widen(sc[d]))", "round_bf16(1.0f - widen(sc[d]))"),
+    ("folded_shift_dropped", "out[r * D + d] = round_bf16(scaled + widen(sh[d]));",
+     "out[r * D + d] = round_bf16(scaled);"),
+    ("folded_normed_rounded", "float scaled = normed * w;",
+     "float scaled = widen(round_bf16(normed)) * w;"),
 ]
 
 
@@ -64,6 +71,7 @@ def pins_fail(lib):
            os.path.join(ROOT, "tests", "test_oracle_chains.py"),
            os.path.join(ROOT, "tests", "test_oracle_stats.py"),
            os.path.join(ROOT, "tests", "test_oracle_ops.py"),
+           os.path.join(ROOT, "tests", "test_oracle_folded.py"),
            "-k", "not exhaustive"]
     res = subprocess.run(cmd, env=env, capture_output=True, text=True, cwd=ROOT)
     return res.returncode != 0

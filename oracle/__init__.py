@@ -15,6 +15,9 @@ Parity status per function (what pins it; see ``tests/test_oracle_*.py``):
   fp32->bf16 cast.
 * ``modulate``, ``residual_gate_add``, ``conv_bias_epilogue``: bit-identical
   to the eager torch bf16 op chain on CPU (the definition the pages give).
+* ``round_f16`` (the C fp32 -> _Float16 conversion): exhaustive over all 2^32
+  fp32 patterns against numpy's float32 -> float16 cast; ``modulate_f16``:
+  bit-identical to the eager torch fp16 chain on CPU.
 * row statistics: against exact rational arithmetic (``fractions``) rounded
   once to fp32, closed forms (constant and zero rows), invariants.
 * ``ln_modulate``, ``rmsnorm_modulate``, ``gated_rmsnorm_modulate``,
@@ -72,6 +75,10 @@ def _load():
             lib.oracle_round_bf16_array.argtypes = [P, P, I]
             lib.oracle_round_bf16_sweep.argtypes = [ctypes.c_uint32, I, P]
             lib.oracle_modulate.argtypes = [P, P, P, P, I, I, I, I]
+            lib.oracle_round_f16.argtypes = [F]
+            lib.oracle_round_f16.restype = ctypes.c_uint16
+            lib.oracle_round_f16_sweep.argtypes = [ctypes.c_uint32, I, P]
+            lib.oracle_modulate_f16.argtypes = [P, P, P, P, I, I, I, I]
             lib.oracle_residual_gate_add.argtypes = [P, P, P, P, I, I, I, I]
             lib.oracle_conv_bias_epilogue.argtypes = [P, P, ctypes.c_int, P, P, I, I]
             lib.oracle_row_stats.argtypes = [P, I, I, P, P, P]
@@ -85,6 +92,7 @@ def _load():
             lib.oracle_qk_layernorm.argtypes = [P, P, P, P, P, P, P, P, I, I, I, F, P, P]
             lib.oracle_rmsnorm_silu_cl.argtypes = [P, P, ctypes.c_int, P, P, I, I, F, P]
             for name in ("oracle_round_bf16_array", "oracle_round_bf16_sweep", "oracle_modulate",
+                         "oracle_round_f16_sweep", "oracle_modulate_f16",
                          "oracle_residual_gate_add", "oracle_conv_bias_epilogue",
                          "oracle_row_stats", "oracle_ln_normalize", "oracle_rms_normalize",
                          "oracle_ln_modulate", "oracle_ln_modulate_folded",
@@ -141,6 +149,13 @@ def round_bf16_sweep(start: int, count: int) -> np.ndarray:
     return out
 
 
+def round_f16_sweep(start: int, count: int) -> np.ndarray:
+    """fp16 bit patterns of the fp32 values with patterns start .. start+count-1."""
+    out = np.empty(count, np.uint16)
+    _load().oracle_round_f16_sweep(ctypes.c_uint32(start), count, _p(out))
+    return out
+
+
 # --------------------------------------------------------------------------
 # elementwise chains
 # --------------------------------------------------------------------------
@@ -154,6 +169,18 @@ def modulate(y, scale, shift):
     assert bs == bs2
     out = np.empty_like(y)
     _load().oracle_modulate(_p(y), _p(sc), _p(sh), _p(out), B, S, D, bs)
+    return out
+
+
+def modulate_f16(y, scale, shift):
+    """fp16 bit patterns: y [B, S, D] -> R16(R16(y * R16(1 + scale)) + shift)."""
+    y = _u16(y)
+    B, S, D = y.shape
+    sc, bs = _mod_rows(scale, B, D)
+    sh, bs2 = _mod_rows(shift, B, D)
+    assert bs == bs2
+    out = np.empty_like(y)
+    _load().oracle_modulate_f16(_p(y), _p(sc), _p(sh), _p(out), B, S, D, bs)
     return out
 
 

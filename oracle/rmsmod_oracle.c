@@ -121,6 +121,61 @@ static bf16_t modulate_one(bf16_t y, bf16_t scale, bf16_t shift)
     return round_bf16(widen(t) + widen(shift));
 }
 
+/* The same chain with fp16 storage ([FLUX] §Accuracy Tests: the modulate
+ * kernel's unit tests cover bf16 and fp16).  R16 is the C language's
+ * fp32 -> _Float16 conversion (IEEE round-to-nearest-even, subnormals kept,
+ * overflow to Inf); widening fp16 -> fp32 is exact. */
+typedef uint16_t f16_t;
+
+static f16_t round_f16(float v)
+{
+    _Float16 h = (_Float16)v;
+    f16_t bits;
+    memcpy(&bits, &h, sizeof bits);
+    return bits;
+}
+
+static float widen_f16(f16_t bits)
+{
+    _Float16 h;
+    memcpy(&h, &bits, sizeof h);
+    return (float)h;
+}
+
+ORACLE_API f16_t oracle_round_f16(float v) { return round_f16(v); }
+
+ORACLE_API float oracle_widen_f16(f16_t h) { return widen_f16(h); }
+
+/* Round the fp32 values whose bit patterns are start, ..., start+count-1 to fp16. */
+ORACLE_API void oracle_round_f16_sweep(uint32_t start, int64_t count, f16_t* out)
+{
+    for (int64_t i = 0; i < count; ++i) {
+        uint32_t u = start + (uint32_t)i;
+        float v;
+        memcpy(&v, &u, sizeof v);
+        out[i] = round_f16(v);
+    }
+}
+
+/* out = R16(f(R16(f(y) * f(R16(1 + f(scale))))) + f(shift)) over [B, S, D]. */
+ORACLE_API void oracle_modulate_f16(const f16_t* y, const f16_t* scale, const f16_t* shift,
+                                    f16_t* out, int64_t B, int64_t S, int64_t D,
+                                    int64_t mod_bstride)
+{
+    for (int64_t b = 0; b < B; ++b) {
+        const f16_t* sc = scale + b * mod_bstride;
+        const f16_t* sh = shift + b * mod_bstride;
+        for (int64_t s = 0; s < S; ++s) {
+            int64_t row = (b * S + s) * D;
+            for (int64_t d = 0; d < D; ++d) {
+                f16_t one_plus = round_f16(1.0f + widen_f16(sc[d]));
+                f16_t t = round_f16(widen_f16(y[row + d]) * widen_f16(one_plus));
+                out[row + d] = round_f16(widen_f16(t) + widen_f16(sh[d]));
+            }
+        }
+    }
+}
+
 /* res = R(f(residual) + f(R(f(gate) * f(update))))
  * The eager pair round(gate*update), round(residual + ...): [ERNIE] §What
  * "rounding-faithful" means here (residual variant); [GLM] §Motivation (ff gate). */

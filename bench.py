@@ -595,6 +595,19 @@ def kernel_table(rm, lib, dev, stream, l2, peak, iters=200, only=None):
                for a, o in zip(xs, os_)])
         del xs, os_
 
+    # the single-rounding tier on the CFG pair
+    name = "ln_modulate_folded_flux_2x4608x3072"
+    if want(name):
+        B, S, D = 2, 4608, 3072
+        n = nsets_for(B * S * D * 4)
+        xs = [normal((B, S, D)) for _ in range(n)]
+        sc, sh = normal((B, 1, D), 0.1), normal((B, 1, D), 0.1)
+        os_ = [torch.empty_like(xs[0]) for _ in range(n)]
+        timed(name, B * S * D * 4 + 2 * B * D * 2, B * S,
+              [lambda a=a, o=o: rm.ln_modulate_folded(a, sc, sh, out=o, stream=stream)
+               for a, o in zip(xs, os_)])
+        del xs, os_
+
     # RMSNorm + modulate and the gated site, ERNIE-Image
     S, D = 4216, 4096
     w = normal((D,), 0.05, 1.0)

@@ -90,6 +90,26 @@ int ln_modulate(const void* x, const void* scale, const void* shift, void* out,
                 float* mean_out, float* rstd_out, rmsmod_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * ln_modulate_folded -- single-rounding tier of ln_modulate (not bit-exact
+ * with the eager chain).
+ *   [FLUX] §Modifications commit 3 (quality="high": the modulate folds into
+ *   the LayerNorm's elementwise affine, layer_norm(x, weight = 1 + scale,
+ *   bias = shift), with 1 + scale keeping the eager rounding of its row;
+ *   max abs difference to the lossless chain at the bf16 rounding level).
+ *
+ *   Statistics, rstd, arguments, layout, aliasing and errors as ln_modulate;
+ *   per element
+ *     w          = R(1 + f(scale_b[d]))
+ *     out[r, d]  = R(((f(x[r,d]) - mean) * rstd) * f(w) + f(shift_b[d]))
+ *   in fp32 with each operation rounded separately (no FMA) and one final
+ *   rounding to bf16.  Unlike the page's aten route it takes per-batch
+ *   modulation rows (mod_bstride) for B > 1.
+ * ---------------------------------------------------------------------- */
+int ln_modulate_folded(const void* x, const void* scale, const void* shift, void* out,
+                       int64_t B, int64_t S, int64_t D, int64_t mod_bstride, float eps,
+                       float* mean_out, float* rstd_out, rmsmod_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * rmsnorm_modulate -- RMSNorm (optional weight), then the modulate chain.
  *   [ERNIE] §What "rounding-faithful" means here (rstd from sum_sq / H + eps;
  *   one final rounding of x * rstd * w; the aten modulate chain).
@@ -166,6 +186,15 @@ int modulate_scale_shift(const void* y, const void* scale, const void* shift, vo
                          int64_t B, int64_t S, int64_t D, int64_t mod_bstride,
                          rmsmod_stream_t stream);
 
+/* modulate_scale_shift_f16: the same chain on fp16 storage, R16 = fp32 -> fp16
+ * round-to-nearest-even (subnormals kept, overflow to Inf), every operand and
+ * result an IEEE binary16 bit pattern; arguments, layout, aliasing and errors
+ * as modulate_scale_shift.
+ *   [FLUX] §Accuracy Tests (the modulate kernel covers bf16 and fp16). */
+int modulate_scale_shift_f16(const void* y, const void* scale, const void* shift, void* out,
+                             int64_t B, int64_t S, int64_t D, int64_t mod_bstride,
+                             rmsmod_stream_t stream);
+
 /* residual_gate_add: res = R(f(residual) + f(R(f(gate_b) * f(update)))) over [B, S, D].
  *   [GLM] §Motivation (ff gate) and [ERNIE] §What (residual variant). */
 int residual_gate_add(const void* residual, const void* gate, const void* update,
@@ -187,7 +216,8 @@ enum {
     RMSMOD_OP_RMSNORM_MODULATE = 2,
     RMSMOD_OP_GATED_RMSNORM_MODULATE = 3,
     RMSMOD_OP_QK_LAYERNORM = 4,
-    RMSMOD_OP_RMSNORM_SILU_CL = 5
+    RMSMOD_OP_RMSNORM_SILU_CL = 5,
+    RMSMOD_OP_LN_MODULATE_FOLDED = 6
 };
 
 /* 1 if `op` supports row length / channel count `D_or_C` and every non-NULL

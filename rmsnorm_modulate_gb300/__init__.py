@@ -21,11 +21,12 @@ import threading
 import torch
 
 __all__ = [
-    "RmsmodError", "library", "library_path", "ln_modulate", "rmsnorm_modulate",
+    "RmsmodError", "library", "library_path", "ln_modulate", "ln_modulate_folded",
+    "rmsnorm_modulate",
     "gated_rmsnorm_modulate", "qk_layernorm", "rmsnorm_silu_cl", "modulate_scale_shift",
     "residual_gate_add", "conv_bias_epilogue", "supported", "status_string", "device_status",
     "OP_LN_MODULATE", "OP_RMSNORM_MODULATE", "OP_GATED_RMSNORM_MODULATE",
-    "OP_QK_LAYERNORM", "OP_RMSNORM_SILU_CL",
+    "OP_QK_LAYERNORM", "OP_RMSNORM_SILU_CL", "OP_LN_MODULATE_FOLDED",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -36,6 +37,7 @@ OP_RMSNORM_MODULATE = 2
 OP_GATED_RMSNORM_MODULATE = 3
 OP_QK_LAYERNORM = 4
 OP_RMSNORM_SILU_CL = 5
+OP_LN_MODULATE_FOLDED = 6
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +69,8 @@ def library() -> ctypes.CDLL:
         P, I, F, C = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
         sig = {
             "ln_modulate": [P, P, P, P, I, I, I, I, F, P, P, P],
+            "ln_modulate_folded": [P, P, P, P, I, I, I, I, F, P, P, P],
+            "modulate_scale_shift_f16": [P, P, P, P, I, I, I, I, P],
             "rmsnorm_modulate": [P, P, P, P, P, I, I, I, I, F, P, P],
             "gated_rmsnorm_modulate": [P, P, P, I, P, P, P, I, P, P, I, I, I, F, P, P],
             "qk_layernorm": [P, P, P, P, P, P, P, P, I, I, I, F, P, P, P],
@@ -108,18 +112,18 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _bf16(t, name):
+def _bf16(t, name, dtype=torch.bfloat16):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.dtype != torch.bfloat16:
-        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_cuda:
         raise ValueError(f"{name} must be on a CUDA device")
     return t
 
 
-def _dense(t, name):
-    _bf16(t, name)
+def _dense(t, name, dtype=torch.bfloat16):
+    _bf16(t, name, dtype)
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t
@@ -133,9 +137,9 @@ def _f32_out(t, n, name, device):
     return t
 
 
-def _mod_rows(t, B, D, name):
+def _mod_rows(t, B, D, name, dtype=torch.bfloat16):
     """-> batch stride in elements (0 = one row shared by every batch)."""
-    _bf16(t, name)
+    _bf16(t, name, dtype)
     if t.shape[-1] != D or t.stride(-1) != 1:
         raise ValueError(f"{name} must end in a unit-stride dimension of size {D}")
     lead = [s for s in t.shape[:-1]]
@@ -153,8 +157,8 @@ def _mod_rows(t, B, D, name):
     raise ValueError(f"{name}: cannot find the batch dimension")
 
 
-def _bsd(x, name="x"):
-    _dense(x, name)
+def _bsd(x, name="x", dtype=torch.bfloat16):
+    _dense(x, name, dtype)
     if x.dim() == 2:
         return 1, x.shape[0], x.shape[1]
     if x.dim() != 3:
@@ -165,7 +169,7 @@ def _bsd(x, name="x"):
 def _out_like(out, x, name="out"):
     if out is None:
         return torch.empty_like(x)
-    _dense(out, name)
+    _dense(out, name, x.dtype)
     if out.shape != x.shape:
         raise ValueError(f"{name} shape {tuple(out.shape)} != {tuple(x.shape)}")
     return out
@@ -182,6 +186,22 @@ def ln_modulate(x, scale, shift, eps: float = 1e-6, out=None, mean_out=None, rst
     _f32_out(mean_out, B * S, "mean_out", x.device)
     _f32_out(rstd_out, B * S, "rstd_out", x.device)
     _call("ln_modulate", _ptr(x), _ptr(scale), _ptr(shift), _ptr(out), B, S, D, bs, eps,
+          _ptr(mean_out), _ptr(rstd_out), _stream(stream))
+    return out
+
+
+def ln_modulate_folded(x, scale, shift, eps: float = 1e-6, out=None, mean_out=None,
+                       rstd_out=None, stream=None):
+    """Single-rounding tier: R(((x - mean) * rstd) * R(1 + scale) + shift) (not bit-exact
+    with the eager chain; same arguments as ln_modulate)."""
+    B, S, D = _bsd(x)
+    bs = _mod_rows(scale, B, D, "scale")
+    if _mod_rows(shift, B, D, "shift") != bs:
+        raise ValueError("scale and shift must share one batch stride")
+    out = _out_like(out, x)
+    _f32_out(mean_out, B * S, "mean_out", x.device)
+    _f32_out(rstd_out, B * S, "rstd_out", x.device)
+    _call("ln_modulate_folded", _ptr(x), _ptr(scale), _ptr(shift), _ptr(out), B, S, D, bs, eps,
           _ptr(mean_out), _ptr(rstd_out), _stream(stream))
     return out
 
@@ -288,14 +308,18 @@ def rmsnorm_silu_cl(x, bias, gamma, eps: float = 1e-6, out=None, rstd_out=None, 
 
 
 def modulate_scale_shift(y, scale, shift, out=None, stream=None):
-    """R(R(y * R(1 + scale)) + shift) over y [B, S, D]."""
-    B, S, D = _bsd(y, "y")
-    bs = _mod_rows(scale, B, D, "scale")
-    if _mod_rows(shift, B, D, "shift") != bs:
+    """R(R(y * R(1 + scale)) + shift) over y [B, S, D], in y's storage type
+    (bfloat16 or float16; scale and shift must match it)."""
+    if isinstance(y, torch.Tensor) and y.dtype == torch.float16:
+        dt, entry = torch.float16, "modulate_scale_shift_f16"
+    else:
+        dt, entry = torch.bfloat16, "modulate_scale_shift"
+    B, S, D = _bsd(y, "y", dt)
+    bs = _mod_rows(scale, B, D, "scale", dt)
+    if _mod_rows(shift, B, D, "shift", dt) != bs:
         raise ValueError("scale and shift must share one batch stride")
     out = _out_like(out, y)
-    _call("modulate_scale_shift", _ptr(y), _ptr(scale), _ptr(shift), _ptr(out), B, S, D, bs,
-          _stream(stream))
+    _call(entry, _ptr(y), _ptr(scale), _ptr(shift), _ptr(out), B, S, D, bs, _stream(stream))
     return out
 
 

@@ -151,6 +151,7 @@ RMSMOD_EXPORT int rmsmod_supported(int op, int64_t D_or_C, const void* const* pt
         return 0;
     switch (op) {
     case RMSMOD_OP_LN_MODULATE:
+    case RMSMOD_OP_LN_MODULATE_FOLDED:
     case RMSMOD_OP_RMSNORM_MODULATE:
     case RMSMOD_OP_GATED_RMSNORM_MODULATE:
         if (D_or_C > RMSMOD_MAX_D)
@@ -175,9 +176,9 @@ RMSMOD_EXPORT int rmsmod_supported(int op, int64_t D_or_C, const void* const* pt
     return 1;
 }
 
-RMSMOD_EXPORT int ln_modulate(const void* x, const void* scale, const void* shift, void* out,
-                              int64_t B, int64_t S, int64_t D, int64_t mod_bstride, float eps,
-                              float* mean_out, float* rstd_out, rmsmod_stream_t stream)
+static int ln_modulate_op(int op, const void* x, const void* scale, const void* shift, void* out,
+                          int64_t B, int64_t S, int64_t D, int64_t mod_bstride, float eps,
+                          float* mean_out, float* rstd_out, rmsmod_stream_t stream)
 {
     int st = check_bsd(B, S, D);
     if (st != RMSMOD_OK)
@@ -214,7 +215,24 @@ RMSMOD_EXPORT int ln_modulate(const void* x, const void* scale, const void* shif
     a.n = static_cast<float>(D);
     a.inv_n = 1.0f / static_cast<float>(D);
     a.eps = eps;
-    return launch_status(rmsmod::launch_row_kernel(rmsmod::kOpLN, a, dev, stream));
+    return launch_status(rmsmod::launch_row_kernel(op, a, dev, stream));
+}
+
+RMSMOD_EXPORT int ln_modulate(const void* x, const void* scale, const void* shift, void* out,
+                              int64_t B, int64_t S, int64_t D, int64_t mod_bstride, float eps,
+                              float* mean_out, float* rstd_out, rmsmod_stream_t stream)
+{
+    return ln_modulate_op(rmsmod::kOpLN, x, scale, shift, out, B, S, D, mod_bstride, eps,
+                          mean_out, rstd_out, stream);
+}
+
+RMSMOD_EXPORT int ln_modulate_folded(const void* x, const void* scale, const void* shift,
+                                     void* out, int64_t B, int64_t S, int64_t D,
+                                     int64_t mod_bstride, float eps, float* mean_out,
+                                     float* rstd_out, rmsmod_stream_t stream)
+{
+    return ln_modulate_op(rmsmod::kOpLNFold, x, scale, shift, out, B, S, D, mod_bstride, eps,
+                          mean_out, rstd_out, stream);
 }
 
 RMSMOD_EXPORT int rmsnorm_modulate(const void* x, const void* weight, const void* scale,
@@ -420,9 +438,9 @@ int check_ew_rows(int64_t rows, int64_t D)
 
 }  // namespace
 
-RMSMOD_EXPORT int modulate_scale_shift(const void* y, const void* scale, const void* shift,
-                                       void* out, int64_t B, int64_t S, int64_t D,
-                                       int64_t mod_bstride, rmsmod_stream_t stream)
+static int modulate_op(int op, const void* y, const void* scale, const void* shift, void* out,
+                       int64_t B, int64_t S, int64_t D, int64_t mod_bstride,
+                       rmsmod_stream_t stream)
 {
     if (B < 0 || S < 0 || (B != 0 && S > INT64_MAX / B))
         return RMSMOD_ERR_SHAPE;
@@ -455,7 +473,22 @@ RMSMOD_EXPORT int modulate_scale_shift(const void* y, const void* scale, const v
     a.rows = B * S;
     a.S = S;
     a.Dv = static_cast<int>(D / 8);
-    return launch_status(rmsmod::launch_elementwise(rmsmod::kEwModulate, a, dev, stream));
+    return launch_status(rmsmod::launch_elementwise(op, a, dev, stream));
+}
+
+RMSMOD_EXPORT int modulate_scale_shift(const void* y, const void* scale, const void* shift,
+                                       void* out, int64_t B, int64_t S, int64_t D,
+                                       int64_t mod_bstride, rmsmod_stream_t stream)
+{
+    return modulate_op(rmsmod::kEwModulate, y, scale, shift, out, B, S, D, mod_bstride, stream);
+}
+
+RMSMOD_EXPORT int modulate_scale_shift_f16(const void* y, const void* scale, const void* shift,
+                                           void* out, int64_t B, int64_t S, int64_t D,
+                                           int64_t mod_bstride, rmsmod_stream_t stream)
+{
+    return modulate_op(rmsmod::kEwModulateF16, y, scale, shift, out, B, S, D, mod_bstride,
+                       stream);
 }
 
 RMSMOD_EXPORT int residual_gate_add(const void* residual, const void* gate, const void* update,

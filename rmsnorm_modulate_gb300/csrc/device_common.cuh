@@ -216,6 +216,26 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi)
 
 constexpr uint32_t kBf2One = 0x3F803F80u;  // (1.0, 1.0)
 
+// Packed fp16 (IEEE binary16, subnormals kept): correctly rounded add and
+// multiply, which for fp16 operands equal "fp32 op, then round to fp16" (the
+// product is exact in fp32; for the sum fp32 carries more than 2 * 11 + 2
+// bits, so the double rounding is innocuous).
+__device__ __forceinline__ uint32_t h2_add(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+constexpr uint32_t kH2One = 0x3C003C00u;  // (1.0, 1.0) in fp16
+
 // R(f(v) + f(c)) for the eight bf16 of a vector against a bf16x2 constant.
 __device__ __forceinline__ uint4 bf2x4_add(uint4 v, uint32_t c)
 {

@@ -1,7 +1,8 @@
 // Standalone bit-exact elementwise chains on sm_103a: the fused kernels'
 // modulate epilogue, gated-residual prologue and conv-bias fold, exported on
 // their own.
-//   modulate_scale_shift: sglang #34004 FLUX.1, §Modifications commit 2
+//   modulate_scale_shift (bf16 and fp16): sglang #34004 FLUX.1, §Modifications
+//                         commit 2 and §Accuracy Tests
 //   residual_gate_add:    sglang #33854 ERNIE-Image residual variant; #34008 ff gate
 //   conv_bias_epilogue:   sglang #38650 Wan VAE, §New kernel, lossless
 //
@@ -32,6 +33,14 @@ __device__ __forceinline__ uint4 apply(const EwArgs& a, uint32_t i, const FastDi
 #pragma unroll
         for (int k = 0; k < 4; ++k)
             word(o, k) = bf2_add(bf2_mul(word(av, k), bf2_add(word(s, k), kBf2One)), word(h, k));
+    } else if (OP == kEwModulateF16) {
+        const uint32_t b = fd_batch.div(row);
+        const int64_t off = static_cast<int64_t>(b) * a.bstride + c;
+        uint4 s = ld_cached(static_cast<const uint4*>(a.b) + off);
+        uint4 h = ld_cached(static_cast<const uint4*>(a.c) + off);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            word(o, k) = h2_add(h2_mul(word(av, k), h2_add(word(s, k), kH2One)), word(h, k));
     } else if (OP == kEwGateAdd) {
         const uint32_t b = fd_batch.div(row);
         uint4 g = ld_cached(static_cast<const uint4*>(a.b) + static_cast<int64_t>(b) * a.bstride + c);
@@ -117,6 +126,8 @@ cudaError_t launch_elementwise(int op, const EwArgs& a, const DeviceInfo& dev,
     switch (op) {
     case kEwModulate:
         return launch<kEwModulate>(a, dev, stream);
+    case kEwModulateF16:
+        return launch<kEwModulateF16>(a, dev, stream);
     case kEwGateAdd:
         return launch<kEwGateAdd>(a, dev, stream);
     default:

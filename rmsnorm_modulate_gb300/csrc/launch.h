@@ -37,7 +37,9 @@ struct FastDiv {
 #endif
 };
 
-enum RowOp : int { kOpLN = 0, kOpRMS = 1, kOpGated = 2 };
+// kOpLNFold: the single-rounding tier of LN + modulate (the modulate folded
+// into the LayerNorm's fp32 affine).
+enum RowOp : int { kOpLN = 0, kOpRMS = 1, kOpGated = 2, kOpLNFold = 3 };
 
 // Every kernel is launched with programmatic stream serialisation: its CTAs
 // may be scheduled while the previous grid in the stream is draining, and the
@@ -120,7 +122,7 @@ struct WanArgs {
 
 cudaError_t launch_wan_kernel(const WanArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
-enum EwOp : int { kEwModulate = 0, kEwGateAdd = 1, kEwBias = 2 };
+enum EwOp : int { kEwModulate = 0, kEwGateAdd = 1, kEwBias = 2, kEwModulateF16 = 3 };
 
 struct EwArgs {
     const void* a;        // y / residual / x

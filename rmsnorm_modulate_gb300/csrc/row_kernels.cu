@@ -170,7 +170,7 @@ struct RowShape {
     // Rows of up to 4096 values keep the per-row re-read vectors in shared
     // memory: R(1 + scale) and shift, plus weight (RMS) and gate (gated).
     static constexpr bool kCached = 32 * V * WPR <= 512;
-    static constexpr int kNmod = OP == kOpLN ? 2 : (OP == kOpRMS ? 3 : 4);
+    static constexpr int kNmod = (OP == kOpLN || OP == kOpLNFold) ? 2 : (OP == kOpRMS ? 3 : 4);
     static constexpr int kCacheBytes = kCached ? kNmod * 32 * V * WPR * 16 : 0;
     // as many warps as ~108 KB per CTA allows, a multiple of WPR; at most 8,
     // or 6 for the larger per-lane rows so three CTAs per SM keep ~110
@@ -191,7 +191,8 @@ struct RowShape {
 };
 
 // out = R(R(y * s1) + shift) for one 16-byte vector, y from x and the row's
-// statistics: the normalise step and the modulate chain.
+// statistics: the normalise step and the modulate chain (or, for the folded
+// tier, the single-rounding affine with weight s1 and bias shift).
 template <int OP>
 __device__ __forceinline__ uint4 normalise_modulate(const uint4& xv, u64 mean2, u64 rstd2,
                                                     const uint4& s1, const uint4& sh,
@@ -202,6 +203,14 @@ __device__ __forceinline__ uint4 normalise_modulate(const uint4& xv, u64 mean2, 
     for (int i = 0; i < 4; ++i) {
         const u64 xx = f2_from_bf2(word(xv, i));
         u64 y;
+        if (OP == kOpLNFold) {
+            // one rounding: R(((x - mean) * rstd) * f(s1) + f(shift)), the
+            // multiply and the add rounded separately
+            const u64 yn = f2_mul(f2_sub(xx, mean2), rstd2);
+            word(o, i) = bf2_from_f2(
+                f2_mul_then_add(yn, f2_from_bf2(word(s1, i)), f2_from_bf2(word(sh, i))));
+            continue;
+        }
         if (OP == kOpLN) {
             y = f2_mul(f2_sub(xx, mean2), rstd2);
         } else {
@@ -238,7 +247,8 @@ __global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads, RowShape<OP, V
     constexpr int kSegVec = Shape::kSegVec;
     constexpr bool kCached = Shape::kCached;
     constexpr int kL = Log2Ceil<8 * V>::value;
-    constexpr bool kNeedSum = (OP == kOpLN);
+    constexpr bool kNeedSum = (OP == kOpLN || OP == kOpLNFold);
+    constexpr bool kWeighted = (OP == kOpRMS || OP == kOpGated);
 
     extern __shared__ __align__(128) uint4 ring[];
     __shared__ __align__(8) unsigned long long bars[kWarps][kStages];
@@ -321,7 +331,7 @@ __global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads, RowShape<OP, V
             for (int c = threadIdx.x; c < Dv; c += blockDim.x) {
                 c_s1[c] = bf2x4_add(ld_cached(scale + b * a.mod_bstride + c), kBf2One);
                 c_sh[c] = ld_cached(shift + b * a.mod_bstride + c);
-                if (OP != kOpLN && has_w)
+                if (kWeighted && has_w)
                     c_w[c] = ld_cached(weight + c);
                 if (OP == kOpGated)
                     c_g[c] = ld_cached(gate + b * a.gate_bstride + c);
@@ -423,12 +433,12 @@ __global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads, RowShape<OP, V
                     if (kCached) {
                         s1 = c_s1[s0 + v];
                         h = c_sh[s0 + v];
-                        if (OP != kOpLN && has_w)
+                        if (kWeighted && has_w)
                             w = c_w[s0 + v];
                     } else {
                         s1 = bf2x4_add(ld_cached(scale + b * a.mod_bstride + s0 + v), kBf2One);
                         h = ld_cached(shift + b * a.mod_bstride + s0 + v);
-                        if (OP != kOpLN && has_w)
+                        if (kWeighted && has_w)
                             w = ld_cached(weight + s0 + v);
                     }
                     st_stream(out + base + v,
@@ -528,6 +538,8 @@ cudaError_t launch_row_kernel(int op, const RowArgs& a, const DeviceInfo& dev,
         return launch_op<kOpLN>(a, dev, stream);
     case kOpRMS:
         return launch_op<kOpRMS>(a, dev, stream);
+    case kOpLNFold:
+        return launch_op<kOpLNFold>(a, dev, stream);
     default:
         return launch_op<kOpGated>(a, dev, stream);
     }

@@ -34,7 +34,7 @@ def header_functions():
 
 def test_header_declares_the_entry_points():
     names = header_functions()
-    for n in ("ln_modulate", "rmsnorm_modulate", "gated_rmsnorm_modulate", "qk_layernorm",
+    for n in ("ln_modulate", "ln_modulate_folded", "rmsnorm_modulate", "gated_rmsnorm_modulate", "qk_layernorm",
               "rmsnorm_silu_cl", "modulate_scale_shift", "residual_gate_add",
               "conv_bias_epilogue", "rmsmod_supported", "rmsmod_status_string",
               "rmsmod_version"):
@@ -70,6 +70,25 @@ MIS = 0x100008
 
 def p(v):
     return P(v)
+
+
+def test_ln_modulate_folded_validation(lib):
+    f = lib.ln_modulate_folded
+    f.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_float, P, P, P]
+    s = P(0)
+    assert f(p(A), p(A + 4096), p(A + 8192), p(A + (1 << 24)), 1, 4, 12, 0, 1e-6, None, None,
+             s) == ERR_SHAPE                                # D % 8
+    assert f(None, p(A + 4096), p(A + 8192), p(A + (1 << 24)), 1, 4, 16, 0, 1e-6, None, None,
+             s) == ERR_NULL
+    assert f(p(MIS), p(A + 4096), p(A + 8192), p(A + (1 << 24)), 1, 4, 16, 0, 1e-6, None,
+             None, s) == ERR_ALIGN
+    assert f(p(A), p(A + 4096), p(A + 8192), p(A + (1 << 24)), 1, 4, 16, 12, 1e-6, None, None,
+             s) == ERR_STRIDE
+    # a partially overlapping output
+    assert f(p(A), p(A + 4096), p(A + 8192), p(A + 16), 1, 4, 16, 0, 1e-6, None, None,
+             s) == ERR_UNSUPPORTED
+    assert lib.rmsmod_supported(6, 3072, None, 0) == 1
 
 
 def test_ln_modulate_validation(lib):

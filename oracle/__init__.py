@@ -23,6 +23,11 @@ Parity status per function (what pins it; see ``tests/test_oracle_*.py``):
 * ``ln_modulate``, ``rmsnorm_modulate``, ``gated_rmsnorm_modulate``,
   ``qk_layernorm``, ``rmsnorm_silu_cl``: fp64 brute force on small rows,
   closed forms, the bias-fold identity, permutation equivariance.
+* ``token_tree_sum`` and ``ln_modulate_backward``: exact integer sums,
+  hand-worked cases where the tree order decides the result, batch
+  invariance; the row reductions c1, c2 against exact rational sums
+  (``fractions``) rounded once; grad_x, grad_scale, grad_shift against torch
+  autograd in fp64; the projection invariants of the LayerNorm backward.
 * ``ln_modulate_folded``: fp64 brute force, torch layer_norm in fp64 with the
   folded weight and bias, closed forms (zero modulation = LayerNorm, weight 2
   doubles it, constant rows give the shift), the bound to the lossless chain.
@@ -91,6 +96,10 @@ def _load():
                                                           I, F, P]
             lib.oracle_qk_layernorm.argtypes = [P, P, P, P, P, P, P, P, I, I, I, F, P, P]
             lib.oracle_rmsnorm_silu_cl.argtypes = [P, P, ctypes.c_int, P, P, I, I, F, P]
+            lib.oracle_token_tree_sum.argtypes = [P, I, P]
+            lib.oracle_token_tree_sum.restype = F
+            lib.oracle_ln_modulate_backward.argtypes = [P, P, P, P, P, I, I, I, I, P, P, P, P,
+                                                        P, P]
             for name in ("oracle_round_bf16_array", "oracle_round_bf16_sweep", "oracle_modulate",
                          "oracle_round_f16_sweep", "oracle_modulate_f16",
                          "oracle_residual_gate_add", "oracle_conv_bias_epilogue",
@@ -98,7 +107,7 @@ def _load():
                          "oracle_ln_modulate", "oracle_ln_modulate_folded",
                          "oracle_rmsnorm_modulate",
                          "oracle_gated_rmsnorm_modulate", "oracle_qk_layernorm",
-                         "oracle_rmsnorm_silu_cl"):
+                         "oracle_rmsnorm_silu_cl", "oracle_ln_modulate_backward"):
                 getattr(lib, name).restype = None
             _lib = lib
     return _lib
@@ -341,3 +350,35 @@ def rmsnorm_silu_cl(x, bias, gamma, eps=1e-6):
     _load().oracle_rmsnorm_silu_cl(_p(x), _p(b), is32, _p(_u16(gamma)), _p(out), pixels, C, eps,
                                    _p(rstd))
     return out, rstd
+
+
+# --------------------------------------------------------------------------
+# backward of LayerNorm + modulate
+# --------------------------------------------------------------------------
+
+def token_tree_sum(v):
+    """Fixed 32-way balanced-tree fp32 sum of a 1-D float32 array."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    scratch = np.empty(max(1, v.size), np.float32)
+    return np.float32(_load().oracle_token_tree_sum(_p(v), v.size, _p(scratch)))
+
+
+def ln_modulate_backward(x, scale, grad_out, mean, rstd):
+    """x, grad_out [B, S, D] bf16 bits; scale [D] / [B, 1, D]; mean, rstd [B*S]
+    (the forward's) -> (grad_x [B, S, D] bf16 bits, grad_scale [B, D] fp32,
+    grad_shift [B, D] fp32, c1 [B*S], c2 [B*S])."""
+    x = _u16(x)
+    B, S, D = x.shape
+    g = np.ascontiguousarray(_u16(grad_out).reshape(B, S, D))
+    sc, bs = _mod_rows(scale, B, D)
+    mean = np.ascontiguousarray(mean, dtype=np.float32).reshape(-1)
+    rstd = np.ascontiguousarray(rstd, dtype=np.float32).reshape(-1)
+    gx = np.empty_like(x)
+    gsc = np.empty((B, D), np.float32)
+    gsh = np.empty((B, D), np.float32)
+    c1 = np.empty(B * S, np.float32)
+    c2 = np.empty(B * S, np.float32)
+    work = np.empty(3 * max(1, S), np.float32)
+    _load().oracle_ln_modulate_backward(_p(x), _p(sc), _p(g), _p(mean), _p(rstd), B, S, D, bs,
+                                        _p(gx), _p(gsc), _p(gsh), _p(c1), _p(c2), _p(work))
+    return gx, gsc, gsh, c1, c2

@@ -521,3 +521,117 @@ ORACLE_API void oracle_rmsnorm_silu_cl(const bf16_t* x, const void* bias, int bi
             rstd_out[p] = rstd;
     }
 }
+
+/* ---------------------------------------------------------------------- */
+/* Backward of LayerNorm (no affine) + modulate ([QWEN] §What: forward and */
+/* backward of out = LayerNorm(x) * (1 + scale) + shift; d_scale and      */
+/* d_shift are token sums reduced by fixed 32-way balanced trees in fp32,  */
+/* applied recursively until one value remains, so the result depends     */
+/* only on the sequence length, not on the batch or the position in it).  */
+/* ---------------------------------------------------------------------- */
+
+/* One 32-way balanced tree: the complete binary tree over 32 slots of fp32
+ * adds, slot i holding v[i] for i < n and +0 beyond. */
+static float tree32(const float* v, int n)
+{
+    float level[32];
+    for (int i = 0; i < 32; ++i)
+        level[i] = i < n ? v[i] : 0.0f;
+    for (int width = 32; width > 1; width /= 2)
+        for (int i = 0; i < width / 2; ++i)
+            level[i] = level[2 * i] + level[2 * i + 1];
+    return level[0];
+}
+
+/* The token sum of n values v[0], v[stride], ...: while more than one value
+ * remains, replace each run of 32 consecutive values (the last run may be
+ * shorter) by its 32-way tree.  scratch holds n floats. */
+static float token_tree_sum(const float* v, int64_t n, int64_t stride, float* scratch)
+{
+    if (n <= 0)
+        return 0.0f;
+    for (int64_t i = 0; i < n; ++i)
+        scratch[i] = v[i * stride];
+    while (n > 1) {
+        int64_t m = (n + 31) / 32;
+        for (int64_t j = 0; j < m; ++j) {
+            int64_t len = n - 32 * j < 32 ? n - 32 * j : 32;
+            scratch[j] = tree32(scratch + 32 * j, (int)len);
+        }
+        n = m;
+    }
+    return scratch[0];
+}
+
+ORACLE_API float oracle_token_tree_sum(const float* v, int64_t n, float* scratch)
+{
+    return token_tree_sum(v, n, 1, scratch);
+}
+
+/* Gradients of out = R(R(y * s1) + shift), y = R(yhat), yhat = (f(x) - mean) * rstd,
+ * s1 = R(1 + f(scale_b)), with the roundings passed straight through:
+ *   dyhat[d]   = f(g[d]) * f(s1[d])                       (exact in fp32)
+ *   c1         = fp32(sum_d dyhat / D),  c2 = fp32(sum_d dyhat * yhat / D)
+ *                (exact sums in double, rounded once)
+ *   grad_x[d]  = R(rstd * ((dyhat - c1) - yhat * c2))     (fp32 ops, no FMA)
+ *   grad_shift[b, d] = T_s(f(g[b, s, d]))
+ *   grad_scale[b, d] = T_s(f(g[b, s, d]) * f(y[b, s, d])) (the products are exact)
+ * with T_s the token tree sum over the S rows of batch b.  mean / rstd are
+ * the forward's per-row statistics.  Any output may be NULL; c1_out / c2_out
+ * (nullable, [B*S]) expose the row reductions for the pins. */
+ORACLE_API void oracle_ln_modulate_backward(const bf16_t* x, const bf16_t* scale,
+                                            const bf16_t* grad_out, const float* mean,
+                                            const float* rstd, int64_t B, int64_t S,
+                                            int64_t D, int64_t mod_bstride, bf16_t* grad_x,
+                                            float* grad_scale, float* grad_shift,
+                                            float* c1_out, float* c2_out, float* work)
+{
+    /* work: 2 * S floats (the token values of one column) + S floats scratch */
+    float* colg = work;
+    float* colgy = work + S;
+    float* scratch = work + 2 * S;
+    for (int64_t b = 0; b < B; ++b) {
+        const bf16_t* sc = scale + b * mod_bstride;
+        for (int64_t s = 0; s < S; ++s) {
+            const int64_t r = b * S + s;
+            const bf16_t* xr = x + r * D;
+            const bf16_t* gr = grad_out + r * D;
+            csum_t a1 = {0.0, 0.0}, a2 = {0.0, 0.0};
+            for (int64_t d = 0; d < D; ++d) {
+                float s1 = widen(round_bf16(1.0f + widen(sc[d])));
+                float yhat = (widen(xr[d]) - mean[r]) * rstd[r];
+                float dy = widen(gr[d]) * s1;
+                csum_add(&a1, (double)dy);
+                csum_add(&a2, (double)dy * (double)yhat);
+            }
+            float c1 = (float)(csum_value(&a1) / (double)D);
+            float c2 = (float)(csum_value(&a2) / (double)D);
+            if (c1_out)
+                c1_out[r] = c1;
+            if (c2_out)
+                c2_out[r] = c2;
+            if (grad_x) {
+                for (int64_t d = 0; d < D; ++d) {
+                    float s1 = widen(round_bf16(1.0f + widen(sc[d])));
+                    float yhat = (widen(xr[d]) - mean[r]) * rstd[r];
+                    float dy = widen(gr[d]) * s1;
+                    float t = (dy - c1) - yhat * c2;
+                    grad_x[r * D + d] = round_bf16(rstd[r] * t);
+                }
+            }
+        }
+        for (int64_t d = 0; d < D; ++d) {
+            for (int64_t s = 0; s < S; ++s) {
+                const int64_t r = b * S + s;
+                float g = widen(grad_out[r * D + d]);
+                float y = widen(round_bf16((widen(x[r * D + d]) - mean[r]) * rstd[r]));
+                colg[s] = g;
+                colgy[s] = g * y;
+            }
+            if (grad_shift)
+                grad_shift[b * D + d] = token_tree_sum(colg, S, 1, scratch);
+            if (grad_scale)
+                grad_scale[b * D + d] = token_tree_sum(colgy, S, 1, scratch);
+        }
+    }
+}

@@ -48,6 +48,16 @@ MUTATIONS = [
      "out[r * D + d] = round_bf16(scaled);"),
     ("folded_normed_rounded", "float scaled = normed * w;",
      "float scaled = widen(round_bf16(normed)) * w;"),
+    ("bwd_no_modulation_factor", "float dy = widen(gr[d]) * s1;\n                csum_add",
+     "float dy = widen(gr[d]);\n                csum_add"),
+    ("bwd_c2_sign", "float t = (dy - c1) - yhat * c2;", "float t = (dy - c1) + yhat * c2;"),
+    ("bwd_c1_dropped", "float t = (dy - c1) - yhat * c2;", "float t = dy - yhat * c2;"),
+    ("bwd_scale_unrounded_y", "float y = widen(round_bf16((widen(x[r * D + d]) - mean[r]) * rstd[r]));",
+     "float y = (widen(x[r * D + d]) - mean[r]) * rstd[r];"),
+    ("bwd_tree_strided_pairs", "level[i] = level[2 * i] + level[2 * i + 1];",
+     "level[i] = level[i] + level[i + width / 2];"),
+    ("bwd_tree_stops_at_one_block", "    while (n > 1) {\n        int64_t m",
+     "    while (n > 32) {\n        int64_t m"),
 ]
 
 
@@ -72,6 +82,7 @@ def pins_fail(lib):
            os.path.join(ROOT, "tests", "test_oracle_stats.py"),
            os.path.join(ROOT, "tests", "test_oracle_ops.py"),
            os.path.join(ROOT, "tests", "test_oracle_folded.py"),
+           os.path.join(ROOT, "tests", "test_oracle_backward.py"),
            "-k", "not exhaustive"]
     res = subprocess.run(cmd, env=env, capture_output=True, text=True, cwd=ROOT)
     return res.returncode != 0

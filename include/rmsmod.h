@@ -42,6 +42,7 @@
 #ifndef RMSMOD_H
 #define RMSMOD_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -108,6 +109,51 @@ int ln_modulate(const void* x, const void* scale, const void* shift, void* out,
 int ln_modulate_folded(const void* x, const void* scale, const void* shift, void* out,
                        int64_t B, int64_t S, int64_t D, int64_t mod_bstride, float eps,
                        float* mean_out, float* rstd_out, rmsmod_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * ln_modulate_backward -- gradients of ln_modulate.
+ *   [QWEN] §What (forward and backward of out = LayerNorm(x, eps, no affine)
+ *   * (1 + scale) + shift; d_scale and d_shift are token sums reduced by
+ *   fixed 32-way balanced fp32 trees applied recursively until one value
+ *   remains, so the result depends only on S, not on B or the batch
+ *   position).
+ *
+ *   With the forward's roundings passed straight through, per row r of
+ *   batch b (mean, rstd: the forward's statistics, as ln_modulate writes
+ *   them to mean_out / rstd_out; s1 = R(1 + f(scale_b))):
+ *     yhat[d]   = (f(x[r,d]) - mean) * rstd           (fp32, as the forward)
+ *     dyhat[d]  = f(grad_out[r,d]) * f(s1[d])          (exact)
+ *     c1, c2    = fp32(sum_d dyhat / D), fp32(sum_d dyhat * yhat / D)
+ *                 (double-float sums, rounded once)
+ *     grad_x    = R(rstd * ((dyhat - c1) - yhat * c2)) (fp32 ops, no FMA)
+ *   and per column d of batch b, over the S rows of the batch:
+ *     grad_shift[b, d] = T(f(grad_out[., d]))
+ *     grad_scale[b, d] = T(f(grad_out[., d]) * f(R(yhat[., d])))
+ *   T: the values are the leaves of a complete binary tree over 32^L slots
+ *   (32^L the smallest power of 32 >= S; slots past S hold +0) summed in
+ *   fp32 with adjacent pairing; S == 1 returns the single value.
+ *
+ *   x, grad_out  bf16 [B*S*D];  scale bf16 rows at base + b * mod_bstride
+ *   mean, rstd   fp32 [B*S], the forward's
+ *   grad_x       nullable bf16 [B*S*D] (must not overlap any input)
+ *   grad_scale, grad_shift  nullable fp32 [B, D] (one row per batch; with a
+ *                shared modulation row the caller sums the rows over b)
+ *   workspace    device memory of at least
+ *                ln_modulate_backward_workspace_bytes(B, S, D) bytes,
+ *                256-byte aligned; needed when grad_scale or grad_shift is
+ *                given (NULL is fine otherwise); owned by the caller,
+ *                overwritten, and in use until the call's work on `stream`
+ *                is done.
+ *   Errors as ln_modulate; RMSMOD_ERR_SHAPE also when workspace_bytes is
+ *   too small.  Three kernel launches on `stream`; nothing is allocated.
+ * ---------------------------------------------------------------------- */
+size_t ln_modulate_backward_workspace_bytes(int64_t B, int64_t S, int64_t D);
+
+int ln_modulate_backward(const void* x, const void* scale, int64_t mod_bstride,
+                         const void* grad_out, const float* mean, const float* rstd,
+                         int64_t B, int64_t S, int64_t D, void* grad_x, float* grad_scale,
+                         float* grad_shift, void* workspace, size_t workspace_bytes,
+                         rmsmod_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * rmsnorm_modulate -- RMSNorm (optional weight), then the modulate chain.

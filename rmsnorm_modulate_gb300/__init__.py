@@ -22,6 +22,7 @@ import torch
 
 __all__ = [
     "RmsmodError", "library", "library_path", "ln_modulate", "ln_modulate_folded",
+    "ln_modulate_backward", "backward_workspace_bytes",
     "rmsnorm_modulate",
     "gated_rmsnorm_modulate", "qk_layernorm", "rmsnorm_silu_cl", "modulate_scale_shift",
     "residual_gate_add", "conv_bias_epilogue", "supported", "status_string", "device_status",
@@ -71,6 +72,7 @@ def library() -> ctypes.CDLL:
             "ln_modulate": [P, P, P, P, I, I, I, I, F, P, P, P],
             "ln_modulate_folded": [P, P, P, P, I, I, I, I, F, P, P, P],
             "modulate_scale_shift_f16": [P, P, P, P, I, I, I, I, P],
+            "ln_modulate_backward": [P, P, I, P, P, P, I, I, I, P, P, P, P, ctypes.c_size_t, P],
             "rmsnorm_modulate": [P, P, P, P, P, I, I, I, I, F, P, P],
             "gated_rmsnorm_modulate": [P, P, P, I, P, P, P, I, P, P, I, I, I, F, P, P],
             "qk_layernorm": [P, P, P, P, P, P, P, P, I, I, I, F, P, P, P],
@@ -204,6 +206,58 @@ def ln_modulate_folded(x, scale, shift, eps: float = 1e-6, out=None, mean_out=No
     _call("ln_modulate_folded", _ptr(x), _ptr(scale), _ptr(shift), _ptr(out), B, S, D, bs, eps,
           _ptr(mean_out), _ptr(rstd_out), _stream(stream))
     return out
+
+
+def backward_workspace_bytes(B: int, S: int, D: int) -> int:
+    """Device workspace ln_modulate_backward needs for the token sums."""
+    lib = library()
+    f = lib.ln_modulate_backward_workspace_bytes
+    f.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
+    f.restype = ctypes.c_size_t
+    return int(f(B, S, D))
+
+
+def ln_modulate_backward(x, scale, grad_out, mean, rstd, need_x=True, need_mod=True,
+                         grad_x=None, grad_scale=None, grad_shift=None, workspace=None,
+                         stream=None):
+    """Gradients of ln_modulate (x, scale rows as in the forward; mean, rstd the
+    forward's fp32 statistics).  -> (grad_x bf16 like x or None, grad_scale fp32
+    [B, D] or None, grad_shift fp32 [B, D] or None).  grad_scale / grad_shift
+    are batch-invariant token sums (fixed 32-way trees); the workspace they need
+    is allocated here unless one is passed."""
+    B, S, D = _bsd(x)
+    bs = _mod_rows(scale, B, D, "scale")
+    _dense(grad_out, "grad_out")
+    if grad_out.shape != x.shape:
+        raise ValueError("grad_out must match x")
+    _f32_out(mean, B * S, "mean", x.device)
+    _f32_out(rstd, B * S, "rstd", x.device)
+    if mean is None or rstd is None:
+        raise ValueError("mean and rstd (the forward's statistics) are required")
+    if need_x:
+        grad_x = _out_like(grad_x, x, "grad_x")
+    else:
+        grad_x = None
+    if need_mod:
+        if grad_scale is None:
+            grad_scale = torch.empty(B, D, dtype=torch.float32, device=x.device)
+        if grad_shift is None:
+            grad_shift = torch.empty(B, D, dtype=torch.float32, device=x.device)
+        _f32_out(grad_scale, B * D, "grad_scale", x.device)
+        _f32_out(grad_shift, B * D, "grad_shift", x.device)
+        need = backward_workspace_bytes(B, S, D)
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+        elif workspace.numel() * workspace.element_size() < need:
+            raise ValueError(f"workspace holds fewer than the {need} bytes needed")
+        wbytes = workspace.numel() * workspace.element_size()
+    else:
+        grad_scale = grad_shift = None
+        workspace, wbytes = None, 0
+    _call("ln_modulate_backward", _ptr(x), _ptr(scale), bs, _ptr(grad_out), _ptr(mean),
+          _ptr(rstd), B, S, D, _ptr(grad_x), _ptr(grad_scale), _ptr(grad_shift),
+          _ptr(workspace), wbytes, _stream(stream))
+    return grad_x, grad_scale, grad_shift
 
 
 def rmsnorm_modulate(x, weight, scale, shift, eps: float = 1e-6, out=None, rstd_out=None,

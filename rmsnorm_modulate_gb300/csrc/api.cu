@@ -134,14 +134,15 @@ RMSMOD_EXPORT int rmsmod_device_status(unsigned int* bits, int clear)
 {
     if (!bits)
         return RMSMOD_ERR_NULL;
-    unsigned a = 0, b = 0, c = 0;
+    unsigned a = 0, b = 0, c = 0, d = 0;
     if (rmsmod::row_kernels_error(&a, clear != 0) != cudaSuccess ||
         rmsmod::qk_kernel_error(&b, clear != 0) != cudaSuccess ||
-        rmsmod::wan_kernel_error(&c, clear != 0) != cudaSuccess) {
+        rmsmod::wan_kernel_error(&c, clear != 0) != cudaSuccess ||
+        rmsmod::backward_error(&d, clear != 0) != cudaSuccess) {
         cudaGetLastError();
         return RMSMOD_ERR_CUDA;
     }
-    *bits = a | b | c;
+    *bits = a | b | c | d;
     return RMSMOD_OK;
 }
 
@@ -233,6 +234,80 @@ RMSMOD_EXPORT int ln_modulate_folded(const void* x, const void* scale, const voi
 {
     return ln_modulate_op(rmsmod::kOpLNFold, x, scale, shift, out, B, S, D, mod_bstride, eps,
                           mean_out, rstd_out, stream);
+}
+
+RMSMOD_EXPORT size_t ln_modulate_backward_workspace_bytes(int64_t B, int64_t S, int64_t D)
+{
+    if (B <= 0 || S <= 0 || D <= 0 || D > RMSMOD_MAX_D || B > INT64_MAX / S)
+        return 0;
+    return rmsmod::backward_workspace_bytes(B, S, D);
+}
+
+RMSMOD_EXPORT int ln_modulate_backward(const void* x, const void* scale, int64_t mod_bstride,
+                                       const void* grad_out, const float* mean,
+                                       const float* rstd, int64_t B, int64_t S, int64_t D,
+                                       void* grad_x, float* grad_scale, float* grad_shift,
+                                       void* workspace, size_t workspace_bytes,
+                                       rmsmod_stream_t stream)
+{
+    int st = check_bsd(B, S, D);
+    if (st != RMSMOD_OK)
+        return st;
+    if ((st = check_bstride(mod_bstride)) != RMSMOD_OK)
+        return st;
+    const int64_t rows = B * S;
+    if (rows == 0 || (!grad_x && !grad_scale && !grad_shift))
+        return RMSMOD_OK;
+    if (!x || !scale || !grad_out || !mean || !rstd)
+        return RMSMOD_ERR_NULL;
+    const bool tokens = grad_scale || grad_shift;
+    if (tokens && !workspace)
+        return RMSMOD_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(scale, 16) || !aligned(grad_out, 16) || !aligned(mean, 4) ||
+        !aligned(rstd, 4) || !aligned(grad_x, 16) || !aligned(grad_scale, 16) ||
+        !aligned(grad_shift, 16) || !aligned(workspace, 256))
+        return RMSMOD_ERR_ALIGN;
+    const size_t need = rmsmod::backward_workspace_bytes(B, S, D);
+    if (tokens && workspace_bytes < need)
+        return RMSMOD_ERR_SHAPE;
+    const int64_t bytes = tensor_bytes(rows, D);
+    const int64_t col_bytes = B * D * 4;
+    // outputs overlap no input and no other output (grad_x may not alias x)
+    const void* ins[] = {x, grad_out};
+    for (const void* in : ins)
+        if (overlap(grad_x, bytes, in, bytes) || overlap(grad_scale, col_bytes, in, bytes) ||
+            overlap(grad_shift, col_bytes, in, bytes) ||
+            (tokens && overlap(workspace, static_cast<int64_t>(need), in, bytes)))
+            return RMSMOD_ERR_UNSUPPORTED;
+    if (overlap(grad_x, bytes, grad_scale, col_bytes) ||
+        overlap(grad_x, bytes, grad_shift, col_bytes) ||
+        overlap(grad_scale, col_bytes, grad_shift, col_bytes) ||
+        (tokens && (overlap(workspace, static_cast<int64_t>(need), grad_x, bytes) ||
+                    overlap(workspace, static_cast<int64_t>(need), grad_scale, col_bytes) ||
+                    overlap(workspace, static_cast<int64_t>(need), grad_shift, col_bytes))) ||
+        overlap(grad_x, bytes, mean, 4 * rows) || overlap(grad_x, bytes, rstd, 4 * rows))
+        return RMSMOD_ERR_UNSUPPORTED;
+    DeviceInfo dev;
+    if ((st = device_info(dev)) != RMSMOD_OK)
+        return st;
+    rmsmod::BwdArgs a{};
+    a.x = x;
+    a.scale = scale;
+    a.mod_bstride = mod_bstride / 8;
+    a.grad_out = grad_out;
+    a.mean = mean;
+    a.rstd = rstd;
+    a.grad_x = grad_x;
+    a.grad_scale = grad_scale;
+    a.grad_shift = grad_shift;
+    a.workspace = workspace;
+    a.B = B;
+    a.S = S;
+    a.Dv = static_cast<int>(D / 8);
+    a.n = static_cast<float>(D);
+    a.inv_n = 1.0f / static_cast<float>(D);
+    a.nblk = (S + 31) / 32;
+    return launch_status(rmsmod::launch_backward(a, dev, stream));
 }
 
 RMSMOD_EXPORT int rmsnorm_modulate(const void* x, const void* weight, const void* scale,

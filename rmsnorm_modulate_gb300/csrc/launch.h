@@ -139,11 +139,36 @@ struct EwArgs {
 cudaError_t launch_elementwise(int op, const EwArgs& a, const DeviceInfo& dev,
                                cudaStream_t stream);
 
+struct BwdArgs {
+    const void* x;         // forward input [B*S*D] bf16
+    const void* scale;     // rows at base + b * mod_bstride
+    int64_t mod_bstride;   // in 8-element vectors
+    const void* grad_out;  // [B*S*D] bf16
+    const float* mean;     // forward statistics [B*S]
+    const float* rstd;
+    void* grad_x;          // nullable [B*S*D] bf16
+    float* grad_scale;     // nullable [B*D]
+    float* grad_shift;     // nullable [B*D]
+    void* workspace;       // [B][nblk][2][D] fp32 when a token sum is wanted
+    int64_t B;
+    int64_t S;
+    int Dv;                // D / 8
+    float n;               // D
+    float inv_n;           // fp32(1 / D)
+    int64_t nblk;          // ceil(S / 32)
+    int64_t items;         // set by the launcher (row kernel work split)
+    int64_t items_per_batch;
+    int64_t chunk;
+};
+size_t backward_workspace_bytes(int64_t B, int64_t S, int64_t D);
+cudaError_t launch_backward(BwdArgs a, const DeviceInfo& dev, cudaStream_t stream);
+
 // Each kernel translation unit keeps a device error word (bit kErrCopyTimeout:
 // an asynchronous copy did not complete in time).  Reads it, optionally
 // clearing it; synchronous.
 cudaError_t row_kernels_error(unsigned* bits, bool clear);
 cudaError_t qk_kernel_error(unsigned* bits, bool clear);
 cudaError_t wan_kernel_error(unsigned* bits, bool clear);
+cudaError_t backward_error(unsigned* bits, bool clear);
 
 }  // namespace rmsmod

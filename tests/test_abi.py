@@ -28,13 +28,14 @@ def lib():
 def header_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:int|char\s*\*|const char\s*\*)\s*\*?\s*"
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char\s*\*|const char\s*\*)\s*\*?\s*"
                                  r"([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_entry_points():
     names = header_functions()
-    for n in ("ln_modulate", "ln_modulate_folded", "rmsnorm_modulate", "gated_rmsnorm_modulate", "qk_layernorm",
+    for n in ("ln_modulate", "ln_modulate_folded", "ln_modulate_backward",
+              "ln_modulate_backward_workspace_bytes", "modulate_scale_shift_f16", "rmsnorm_modulate", "gated_rmsnorm_modulate", "qk_layernorm",
               "rmsnorm_silu_cl", "modulate_scale_shift", "residual_gate_add",
               "conv_bias_epilogue", "rmsmod_supported", "rmsmod_status_string",
               "rmsmod_version"):
@@ -70,6 +71,35 @@ MIS = 0x100008
 
 def p(v):
     return P(v)
+
+
+def test_backward_validation_and_workspace_size(lib):
+    ws = lib.ln_modulate_backward_workspace_bytes
+    ws.argtypes = [ctypes.c_int64] * 3
+    ws.restype = ctypes.c_size_t
+    assert ws(1, 4608, 3072) == 1 * 144 * 2 * 3072 * 4
+    assert ws(2, 33, 64) == 2 * 2 * 2 * 64 * 4
+    assert ws(0, 4, 64) == 0 and ws(1, 0, 64) == 0
+    f = lib.ln_modulate_backward
+    f.argtypes = [P, P, ctypes.c_int64, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                  P, P, P, P, ctypes.c_size_t, P]
+    s = P(0)
+    X, SC, G, M, R = A, A + 4096, A + (1 << 24), A + (2 << 24), A + (3 << 24)
+    GX, GS, GH, W = A + (4 << 24), A + (5 << 24), A + (6 << 24), A + (7 << 24)
+    args = lambda **k: [p(k.get("x", X)), p(k.get("sc", SC)), k.get("bs", 0), p(k.get("g", G)),
+                        p(k.get("m", M)), p(k.get("r", R)), k.get("B", 1), k.get("S", 64),
+                        k.get("D", 64), p(k.get("gx", GX)), p(k.get("gs", GS)),
+                        p(k.get("gh", GH)), p(k.get("w", W)), k.get("wb", 1 << 20), s]
+    assert f(*args(D=12)) == ERR_SHAPE
+    assert f(*args(bs=12)) == ERR_STRIDE
+    assert f(*args(g=0)) == ERR_NULL
+    assert f(*args(w=0)) == ERR_NULL                       # token sums need a workspace
+    assert f(*args(x=MIS)) == ERR_ALIGN
+    assert f(*args(w=A + (7 << 24) + 16)) == ERR_ALIGN     # workspace 256-byte aligned
+    assert f(*args(wb=16)) == ERR_SHAPE                    # workspace too small
+    assert f(*args(gx=X)) == ERR_UNSUPPORTED               # grad_x may not alias x
+    assert f(*args(w=GX)) == ERR_UNSUPPORTED               # workspace overlaps grad_x
+    assert f(*args(gx=0, gs=0, gh=0)) == OK                # nothing requested: no work
 
 
 def test_ln_modulate_folded_validation(lib):

@@ -156,6 +156,30 @@ int ln_modulate_backward(const void* x, const void* scale, int64_t mod_bstride,
                          rmsmod_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * ln_modulate_backward_static -- ln_modulate_backward without a caller
+ * workspace.  The pages have no counterpart: this is a library convenience.
+ *
+ *   Same arguments, results and errors as ln_modulate_backward minus the
+ *   workspace: the token-sum scratch is a fixed 8 MiB (8 << 20 bytes) array
+ *   of the library's own device memory, so the call allocates nothing.
+ *   Sizes whose ln_modulate_backward_workspace_bytes(B, S, D) exceeds
+ *   8 MiB return RMSMOD_ERR_SHAPE and launch nothing (grad_x alone needs no
+ *   scratch and has no such limit).  Nothing in the scratch needs clearing:
+ *   every slot the upper tree levels read is written by the first level of
+ *   the same call.
+ *   Set-up: the first call on a device that asks for a token sum looks the
+ *   array's address up once (it may load the module's device data); make
+ *   that first call outside any stream capture.
+ *   The scratch is one buffer per device: two calls whose work overlaps in
+ *   time (different streams, or host threads issuing at once) race on it and
+ *   give undefined token sums.  Calls on one stream are ordered and safe.
+ * ---------------------------------------------------------------------- */
+int ln_modulate_backward_static(const void* x, const void* scale, int64_t mod_bstride,
+                                const void* grad_out, const float* mean, const float* rstd,
+                                int64_t B, int64_t S, int64_t D, void* grad_x,
+                                float* grad_scale, float* grad_shift, rmsmod_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * rmsnorm_modulate -- RMSNorm (optional weight), then the modulate chain.
  *   [ERNIE] §What "rounding-faithful" means here (rstd from sum_sq / H + eps;
  *   one final rounding of x * rstd * w; the aten modulate chain).

@@ -22,7 +22,7 @@ import torch
 
 __all__ = [
     "RmsmodError", "library", "library_path", "ln_modulate", "ln_modulate_folded",
-    "ln_modulate_backward", "backward_workspace_bytes",
+    "ln_modulate_backward", "ln_modulate_backward_static", "backward_workspace_bytes",
     "rmsnorm_modulate",
     "gated_rmsnorm_modulate", "qk_layernorm", "rmsnorm_silu_cl", "modulate_scale_shift",
     "residual_gate_add", "conv_bias_epilogue", "supported", "status_string", "device_status",
@@ -73,6 +73,7 @@ def library() -> ctypes.CDLL:
             "ln_modulate_folded": [P, P, P, P, I, I, I, I, F, P, P, P],
             "modulate_scale_shift_f16": [P, P, P, P, I, I, I, I, P],
             "ln_modulate_backward": [P, P, I, P, P, P, I, I, I, P, P, P, P, ctypes.c_size_t, P],
+            "ln_modulate_backward_static": [P, P, I, P, P, P, I, I, I, P, P, P, P],
             "rmsnorm_modulate": [P, P, P, P, P, I, I, I, I, F, P, P],
             "gated_rmsnorm_modulate": [P, P, P, I, P, P, P, I, P, P, I, I, I, F, P, P],
             "qk_layernorm": [P, P, P, P, P, P, P, P, I, I, I, F, P, P, P],
@@ -257,6 +258,30 @@ def ln_modulate_backward(x, scale, grad_out, mean, rstd, need_x=True, need_mod=T
     _call("ln_modulate_backward", _ptr(x), _ptr(scale), bs, _ptr(grad_out), _ptr(mean),
           _ptr(rstd), B, S, D, _ptr(grad_x), _ptr(grad_scale), _ptr(grad_shift),
           _ptr(workspace), wbytes, _stream(stream))
+    return grad_x, grad_scale, grad_shift
+
+
+def ln_modulate_backward_static(x, scale, grad_out, mean, rstd, grad_x, grad_scale,
+                                grad_shift, stream=None):
+    """ln_modulate_backward through the entry point that uses the library's
+    fixed 8 MiB device scratch instead of a workspace (allocates nothing; every
+    output is passed in, None to skip it).  Calls overlapping in time race."""
+    B, S, D = _bsd(x)
+    bs = _mod_rows(scale, B, D, "scale")
+    _dense(grad_out, "grad_out")
+    if grad_out.shape != x.shape:
+        raise ValueError("grad_out must match x")
+    if mean is None or rstd is None:
+        raise ValueError("mean and rstd (the forward's statistics) are required")
+    _f32_out(mean, B * S, "mean", x.device)
+    _f32_out(rstd, B * S, "rstd", x.device)
+    if grad_x is not None:
+        _out_like(grad_x, x, "grad_x")
+    _f32_out(grad_scale, B * D, "grad_scale", x.device)
+    _f32_out(grad_shift, B * D, "grad_shift", x.device)
+    _call("ln_modulate_backward_static", _ptr(x), _ptr(scale), bs, _ptr(grad_out), _ptr(mean),
+          _ptr(rstd), B, S, D, _ptr(grad_x), _ptr(grad_scale), _ptr(grad_shift),
+          _stream(stream))
     return grad_x, grad_scale, grad_shift
 
 

@@ -310,6 +310,34 @@ RMSMOD_EXPORT int ln_modulate_backward(const void* x, const void* scale, int64_t
     return launch_status(rmsmod::launch_backward(a, dev, stream));
 }
 
+RMSMOD_EXPORT int ln_modulate_backward_static(const void* x, const void* scale,
+                                              int64_t mod_bstride, const void* grad_out,
+                                              const float* mean, const float* rstd, int64_t B,
+                                              int64_t S, int64_t D, void* grad_x,
+                                              float* grad_scale, float* grad_shift,
+                                              rmsmod_stream_t stream)
+{
+    const bool tokens = grad_scale || grad_shift;
+    void* scratch = nullptr;
+    if (tokens) {
+        int st = check_bsd(B, S, D);
+        if (st != RMSMOD_OK)
+            return st;
+        if (B * S > 0 && rmsmod::backward_workspace_bytes(B, S, D) > rmsmod::kBackwardScratchBytes)
+            return RMSMOD_ERR_SHAPE;
+        DeviceInfo dev;
+        if ((st = device_info(dev)) != RMSMOD_OK)
+            return st;
+        if (rmsmod::backward_static_scratch(dev.device, &scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return RMSMOD_ERR_CUDA;
+        }
+    }
+    return ln_modulate_backward(x, scale, mod_bstride, grad_out, mean, rstd, B, S, D, grad_x,
+                                grad_scale, grad_shift, scratch,
+                                tokens ? rmsmod::kBackwardScratchBytes : 0, stream);
+}
+
 RMSMOD_EXPORT int rmsnorm_modulate(const void* x, const void* weight, const void* scale,
                                    const void* shift, void* out, int64_t B, int64_t S, int64_t D,
                                    int64_t mod_bstride, float eps, float* rstd_out,

@@ -25,6 +25,7 @@
 //   tokens_up      one thread per (batch, column): the trees above the first
 //                  level over the block values, completed to 32^L slots.
 #include <cstddef>
+#include <mutex>
 
 #include "device_common.cuh"
 #include "launch.h"
@@ -338,6 +339,31 @@ __global__ void __launch_bounds__(kTokThreads) tokens_up_kernel(const BwdArgs a)
 }
 
 }  // namespace
+
+// Fixed device scratch for ln_modulate_backward_static: the token-sum
+// workspace of calls whose need fits, in the module's own device memory, so
+// that entry point allocates nothing.  One buffer per device shared by every
+// call: calls whose work overlaps in time (another stream, another host
+// thread) race on it.
+static __device__ __align__(256) unsigned char g_backward_scratch[kBackwardScratchBytes];
+
+cudaError_t backward_static_scratch(int device, void** ptr)
+{
+    static std::mutex mu;
+    static void* addr[64] = {nullptr};
+    const int d = device & 63;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[d]) {
+        // once per device (loads the module's device data if needed)
+        cudaError_t e = cudaGetSymbolAddress(&addr[d], g_backward_scratch);
+        if (e != cudaSuccess) {
+            addr[d] = nullptr;
+            return e;
+        }
+    }
+    *ptr = addr[d];
+    return cudaSuccess;
+}
 
 size_t backward_workspace_bytes(int64_t B, int64_t S, int64_t D)
 {

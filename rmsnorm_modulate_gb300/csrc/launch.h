@@ -161,6 +161,10 @@ struct BwdArgs {
     int64_t chunk;
 };
 size_t backward_workspace_bytes(int64_t B, int64_t S, int64_t D);
+// Size of the fixed device scratch behind ln_modulate_backward_static.
+constexpr size_t kBackwardScratchBytes = size_t(8) << 20;
+// Its address on `device` (looked up once per device, then cached).
+cudaError_t backward_static_scratch(int device, void** ptr);
 cudaError_t launch_backward(BwdArgs a, const DeviceInfo& dev, cudaStream_t stream);
 
 // Each kernel translation unit keeps a device error word (bit kErrCopyTimeout:

@@ -608,6 +608,31 @@ def kernel_table(rm, lib, dev, stream, l2, peak, iters=200, only=None):
                for a, o in zip(xs, os_)])
         del xs, os_
 
+    # backward of LN + modulate (grad_x and the token sums), FLUX.1 B=1 site;
+    # algorithmic bytes: read x and grad_out once, write grad_x once (+ the
+    # fp32 modulation gradients and the per-row statistics)
+    name = "ln_modulate_backward_flux_1x4608x3072"
+    if want(name):
+        B, S, D = 1, 4608, 3072
+        n = nsets_for(B * S * D * 6)
+        xs = [normal((B, S, D)) for _ in range(n)]
+        gs = [normal((B, S, D), 0.5) for _ in range(n)]
+        gxs = [torch.empty_like(xs[0]) for _ in range(n)]
+        sc, sh = normal((B, 1, D), 0.1), normal((B, 1, D), 0.1)
+        means = [torch.empty(B * S, dtype=torch.float32, device=dev) for _ in range(n)]
+        rstds = [torch.empty_like(means[0]) for _ in range(n)]
+        for a, m, r in zip(xs, means, rstds):
+            rm.ln_modulate(a, sc, sh, mean_out=m, rstd_out=r, stream=stream)
+        gsc = torch.empty(B, D, dtype=torch.float32, device=dev)
+        gsh = torch.empty_like(gsc)
+        ws = torch.empty(rm.backward_workspace_bytes(B, S, D), dtype=torch.uint8, device=dev)
+        timed(name, B * S * D * 6 + B * S * 8 + 2 * B * D * 4 + B * D * 2, B * S,
+              [lambda a=a, g=g, o=o, m=m, r=r: rm.ln_modulate_backward(
+                  a, sc, g, m, r, grad_x=o, grad_scale=gsc, grad_shift=gsh, workspace=ws,
+                  stream=stream)
+               for a, g, o, m, r in zip(xs, gs, gxs, means, rstds)])
+        del xs, gs, gxs
+
     # RMSNorm + modulate and the gated site, ERNIE-Image
     S, D = 4216, 4096
     w = normal((D,), 0.05, 1.0)

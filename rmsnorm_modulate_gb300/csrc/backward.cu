@@ -18,10 +18,11 @@
 //                  1-D bulk copies; pass 1 forms c1, c2 as double-float sums
 //                  (TwoSum per value, TwoProd for dyhat * yhat), pass 2
 //                  writes grad_x.
-//   tokens_l1      one thread per (batch, 32-token block, 8 columns): the
-//                  32-way tree of the block in registers (a binary counter
-//                  over the 32 slots, +0 for slots past the end), both
-//                  quantities; the block values go to the workspace.
+//   tokens_l1      four lanes per (batch, 32-token block, 4 columns): each
+//                  lane the tree of 8 token slots in registers (a binary
+//                  counter, +0 for slots past the end), two butterfly steps
+//                  for the top levels, both quantities; the block values go
+//                  to the workspace.
 //   tokens_up      one thread per (batch, column): the trees above the first
 //                  level over the block values, completed to 32^L slots.
 #include <cstddef>
@@ -219,122 +220,199 @@ struct TreeCounter {
 __global__ void __launch_bounds__(kTokThreads) tokens_l1_kernel(const BwdArgs a)
 {
     grid_dependency_sync();
-    // one thread: batch b, block j of 32 tokens, columns 8c .. 8c + 7
-    const int64_t per_batch = static_cast<int64_t>(a.nblk) * a.Dv;
-    const int64_t total = a.B * per_batch;
-    const uint4* __restrict__ xg = static_cast<const uint4*>(a.x);
-    const uint4* __restrict__ gg = static_cast<const uint4*>(a.grad_out);
+    // four consecutive lanes share (batch b, block j of 32 tokens, columns
+    // 4c .. 4c + 3): lane q sums tokens 8q .. 8q + 7 (the slots' three lowest
+    // tree levels), two butterfly steps form the top two levels, so every
+    // lane ends with the block's tree
+    const int cols4 = a.Dv * 2;
+    const int64_t per_batch = static_cast<int64_t>(a.nblk) * cols4;
+    const int64_t total = a.B * per_batch;  // groups of four lanes
+    const uint2* __restrict__ xg = static_cast<const uint2*>(a.x);
+    const uint2* __restrict__ gg = static_cast<const uint2*>(a.grad_out);
     float4* __restrict__ ws = static_cast<float4*>(a.workspace);
-    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
-         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t b = t / per_batch;
-        const int64_t rem = t - b * per_batch;
-        const int64_t j = rem / a.Dv;
-        const int c = static_cast<int>(rem - j * a.Dv);
-        const int64_t s0 = j * 32;
-        const int n = a.S - s0 < 32 ? static_cast<int>(a.S - s0) : 32;
+    const int q = threadIdx.x & 3;
+    const int64_t groups_per_cta = blockDim.x / 4;
+    // every lane of a warp runs the same number of iterations (the shuffles)
+    const int64_t rounds = (total + gridDim.x * groups_per_cta - 1) / (gridDim.x * groups_per_cta);
+    for (int64_t it = 0; it < rounds; ++it) {
+        const int64_t t = (it * gridDim.x + blockIdx.x) * groups_per_cta + (threadIdx.x >> 2);
+        const bool active = t < total;
+        const int64_t tt = active ? t : 0;
+        const int64_t b = tt / per_batch;
+        const int64_t rem = tt - b * per_batch;
+        const int64_t j = rem / cols4;
+        const int c = static_cast<int>(rem - j * cols4);
+        const int64_t s0 = j * 32 + 8 * q;
+        const int n = !active ? 0 : (a.S - s0 < 8 ? (a.S - s0 > 0 ? static_cast<int>(a.S - s0) : 0) : 8);
         const int64_t row0 = b * a.S + s0;
 
-        float rg[8], rp[8];
-        TreeCounter<5> tg[4], tp[4];
+        TreeCounter<3> tg[2], tp[2];
+        u64 raw_g[2] = {0, 0}, raw_p[2] = {0, 0};  // slot 0 (a one-token sequence)
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            u64 gv2[4], pv2[4];
+        for (int k = 0; k < 8; ++k) {
+            u64 gv2[2], pv2[2];
             if (k < n) {
                 const int64_t row = row0 + k;
-                const uint4 xv = ld_stream(xg + row * a.Dv + c);
-                const uint4 gv = ld_stream(gg + row * a.Dv + c);
+                const uint2 xv = ld_stream2(xg + row * cols4 + c);
+                const uint2 gv = ld_stream2(gg + row * cols4 + c);
                 const u64 mean2 = f2_splat(a.mean[row]), rstd2 = f2_splat(a.rstd[row]);
+                const uint32_t xw[2] = {xv.x, xv.y}, gw[2] = {gv.x, gv.y};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const u64 yhat =
-                        f2_mul(f2_sub(f2_from_bf2(word(xv, i)), mean2), rstd2);
+                for (int i = 0; i < 2; ++i) {
+                    const u64 yhat = f2_mul(f2_sub(f2_from_bf2(xw[i]), mean2), rstd2);
                     const u64 y = f2_from_bf2(bf2_from_f2(yhat));
-                    gv2[i] = f2_from_bf2(word(gv, i));
+                    gv2[i] = f2_from_bf2(gw[i]);
                     pv2[i] = f2_mul(gv2[i], y);  // exact: two bf16 values
                 }
-                if (a.S == 1) {
-                    // a sequence of one token: its value as is, no tree
+                if (k == 0) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        f2_unpack(gv2[i], rg[2 * i], rg[2 * i + 1]);
-                        f2_unpack(pv2[i], rp[2 * i], rp[2 * i + 1]);
+                    for (int i = 0; i < 2; ++i) {
+                        raw_g[i] = gv2[i];
+                        raw_p[i] = pv2[i];
                     }
                 }
             } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < 2; ++i)
                     gv2[i] = pv2[i] = 0;  // +0 past the end of the sequence
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 2; ++i) {
                 tg[i].push(k, gv2[i]);
                 tp[i].push(k, pv2[i]);
             }
         }
-        if (a.S != 1) {
+        u64 vg[2], vp[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                f2_unpack(tg[i].stack[4], rg[2 * i], rg[2 * i + 1]);
-                f2_unpack(tp[i].stack[4], rp[2 * i], rp[2 * i + 1]);
+        for (int i = 0; i < 2; ++i) {
+            if (a.S == 1) {
+                // a sequence of one token: its value as is, no tree (lane 0 of
+                // the group holds it and is the one that writes)
+                vg[i] = raw_g[i];
+                vp[i] = raw_p[i];
+                continue;
+            }
+            vg[i] = tg[i].stack[2];
+            vp[i] = tp[i].stack[2];
+            // levels 3 and 4: (T0 + T1) + (T2 + T3), the left operand the
+            // earlier tokens (the adds are commutative, so every lane agrees)
+#pragma unroll
+            for (int off = 1; off <= 2; off <<= 1) {
+                const u64 og = __shfl_xor_sync(kFullMask, vg[i], off);
+                const u64 op = __shfl_xor_sync(kFullMask, vp[i], off);
+                const bool left = (q & off) == 0;
+                vg[i] = left ? f2_add(vg[i], og) : f2_add(og, vg[i]);
+                vp[i] = left ? f2_add(vp[i], op) : f2_add(op, vp[i]);
             }
         }
-        // workspace [B][nblk][2][D] fp32: quantity 0 = grad_shift, 1 = grad_scale
-        const int64_t o = ((b * a.nblk + j) * 2) * (a.Dv * 2) + 2 * c;
-        ws[o] = make_float4(rg[0], rg[1], rg[2], rg[3]);
-        ws[o + 1] = make_float4(rg[4], rg[5], rg[6], rg[7]);
-        ws[o + 2 * a.Dv] = make_float4(rp[0], rp[1], rp[2], rp[3]);
-        ws[o + 2 * a.Dv + 1] = make_float4(rp[4], rp[5], rp[6], rp[7]);
+        if (active && q == 0) {
+            float rg[4], rp[4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                f2_unpack(vg[i], rg[2 * i], rg[2 * i + 1]);
+                f2_unpack(vp[i], rp[2 * i], rp[2 * i + 1]);
+            }
+            // workspace [B][nblk][2][D] fp32: quantity 0 = grad_shift, 1 = grad_scale
+            const int64_t o = ((b * a.nblk + j) * 2) * static_cast<int64_t>(cols4) + c;
+            ws[o] = make_float4(rg[0], rg[1], rg[2], rg[3]);
+            ws[o + cols4] = make_float4(rp[0], rp[1], rp[2], rp[3]);
+        }
     }
 }
 
-// Above the first level: the block values of one column form the leaves of
-// a complete binary tree over 32^L' slots (L' = levels still needed, the
-// slots past nblk hold +0); a binary counter in local memory walks them.
+// Above the first level: the block values of one column are the leaves of a
+// complete binary tree over 32^L slots (32^L >= nblk, slots past nblk +0).
+// Each run of 32 block values is one level-2 node: its 32 loads are issued
+// together and combined by a register binary counter; the level-2 nodes then
+// go through a small counter in local memory, completed with +0 subtrees.
+template <int LEVELS>
+struct ScalarTree {
+    float stack[LEVELS];
+
+    __device__ __forceinline__ void push(int k, float v)
+    {
+#pragma unroll
+        for (int l = 0; l < LEVELS; ++l) {
+            if (((k >> l) & 1) == 0) {
+                stack[l] = v;
+                return;
+            }
+            v = __fadd_rn(stack[l], v);
+        }
+        stack[LEVELS - 1] = v;
+    }
+};
+
 __global__ void __launch_bounds__(kTokThreads) tokens_up_kernel(const BwdArgs a)
 {
     grid_dependency_sync();
     const int D = a.Dv * 8;
     const int64_t total = a.B * static_cast<int64_t>(D);
     const float* __restrict__ ws = static_cast<const float*>(a.workspace);
+    const int64_t nblk = a.nblk;
+    const int64_t n2 = (nblk + 31) / 32;
+    int K2 = 0;  // levels of the tree over the level-2 nodes: 2^K2 = 32^L2 >= n2
+    for (int64_t cap = 1; cap < n2; cap *= 32)
+        K2 += 5;
+    const int64_t stride = 2 * static_cast<int64_t>(D);
     for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
          t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t b = t / D;
         const int d = static_cast<int>(t - b * D);
-        float res[2];
-        for (int q = 0; q < 2; ++q) {
-            const float* col = ws + (b * a.nblk * 2 + q) * static_cast<int64_t>(D) + d;
-            const int64_t stride = 2 * static_cast<int64_t>(D);
-            if (a.nblk == 1) {
-                res[q] = col[0];
-                continue;
-            }
-            // K = 5 * L' levels: the smallest 32^L' >= nblk
-            int K = 0;
-            for (int64_t cap = 1; cap < a.nblk; cap *= 32)
-                K += 5;
-            float stack[64];
-            for (int64_t k = 0; k < a.nblk; ++k) {
-                float v = col[k * stride];
+        const float* col0 = ws + (b * nblk * 2) * static_cast<int64_t>(D) + d;  // quantity 0
+        const float* col1 = col0 + D;                                          // quantity 1
+        float res0, res1;
+        if (nblk == 1) {
+            res0 = col0[0];
+            res1 = col1[0];
+        } else {
+            float st0[32], st1[32];  // counter over the level-2 nodes (K2 <= 30)
+            for (int64_t m = 0; m < n2; ++m) {
+                ScalarTree<5> t0, t1;
+                float v0[32], v1[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const int64_t idx = 32 * m + k;
+                    v0[k] = idx < nblk ? col0[idx * stride] : 0.0f;
+                    v1[k] = idx < nblk ? col1[idx * stride] : 0.0f;
+                }
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    t0.push(k, v0[k]);
+                    t1.push(k, v1[k]);
+                }
+                float u0 = t0.stack[4], u1 = t1.stack[4];
                 int l = 0;
-                for (; (k >> l) & 1; ++l)
-                    v = __fadd_rn(stack[l], v);
-                stack[l] = v;
+                for (; (m >> l) & 1; ++l) {
+                    u0 = __fadd_rn(st0[l], u0);
+                    u1 = __fadd_rn(st1[l], u1);
+                }
+                st0[l] = u0;
+                st1[l] = u1;
             }
-            // complete the tree: slots nblk .. 2^K - 1 hold +0
-            float carry = 0.0f;
-            for (int l = 0; l < K; ++l) {
-                if ((a.nblk >> l) & 1)
-                    carry = __fadd_rn(stack[l], carry);  // finished left subtree + the rest
-                else
-                    carry = __fadd_rn(carry, 0.0f);       // the rest + an all-zero subtree
+            if (K2 == 0) {
+                res0 = st0[0];
+                res1 = st1[0];
+            } else {
+                // complete the tree: level-2 slots n2 .. 2^K2 - 1 hold +0
+                float c0 = 0.0f, c1 = 0.0f;
+                for (int l = 0; l < K2; ++l) {
+                    if ((n2 >> l) & 1) {
+                        c0 = __fadd_rn(st0[l], c0);  // finished left subtree + the rest
+                        c1 = __fadd_rn(st1[l], c1);
+                    } else {
+                        c0 = __fadd_rn(c0, 0.0f);    // the rest + an all-zero subtree
+                        c1 = __fadd_rn(c1, 0.0f);
+                    }
+                }
+                res0 = c0;
+                res1 = c1;
             }
-            res[q] = carry;
         }
         if (a.grad_shift)
-            a.grad_shift[t] = res[0];
+            a.grad_shift[t] = res0;
         if (a.grad_scale)
-            a.grad_scale[t] = res[1];
+            a.grad_scale[t] = res1;
     }
 }
 
@@ -411,9 +489,9 @@ cudaError_t launch_backward(BwdArgs a, const DeviceInfo& dev, cudaStream_t strea
             return e;
     }
     if (a.grad_scale || a.grad_shift) {
-        const int64_t l1 = a.B * a.nblk * a.Dv;
+        const int64_t l1 = a.B * a.nblk * a.Dv * 2 * 4;  // four lanes per group
         int64_t g1 = (l1 + kTokThreads - 1) / kTokThreads;
-        const int64_t cap = static_cast<int64_t>(dev.sms) * 8;
+        const int64_t cap = static_cast<int64_t>(dev.sms) * 12;
         e = launch_dependent(tokens_l1_kernel, static_cast<int>(g1 < cap ? g1 : cap),
                              kTokThreads, 0, stream, a);
         if (e != cudaSuccess)

@@ -30,6 +30,14 @@ constexpr unsigned kFullMask = 0xFFFFFFFFu;
 
 // Streaming 16-byte load of data touched once (no L1 allocation).  The
 // coherent path, not the read-only one: an output may alias its input.
+// 8-byte read-only streaming load (input never written by the same kernel).
+__device__ __forceinline__ uint2 ld_stream2(const uint2* p)
+{
+    uint2 v;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ uint4 ld_stream(const uint4* p)
 {
     uint4 v;

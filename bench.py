@@ -678,6 +678,21 @@ def kernel_table(rm, lib, dev, stream, l2, peak, iters=200, only=None):
                for a, b, c, d in zip(qs, ks, qo, ko)])
         del qs, ks, qo, ko
 
+    # the same site on q / k slices of a fused QKV projection [S, 3, 32, 128],
+    # normalised in place inside the buffer
+    name = "qk_layernorm_qkv_strided_1x4352x32x128"
+    if want(name):
+        T, H, hd = 4352 * 1, 32, 128
+        n = nsets_for(3 * T * H * hd * 2)
+        qkvs = [normal((T, 3, H, hd), 2.0) for _ in range(n)]
+        wq, bq = normal((hd,), 0.05, 1.0), normal((hd,), 0.02)
+        wk, bk = normal((hd,), 0.05, 1.0), normal((hd,), 0.02)
+        timed(name, 2 * T * H * hd * 4 + 4 * hd * 2, 2 * T * H,
+              [lambda t=t: rm.qk_layernorm(t[:, 0], t[:, 1], wq, bq, wk, bk, q_out=t[:, 0],
+                                           k_out=t[:, 1], stream=stream)
+               for t in qkvs])
+        del qkvs
+
     # channels-last RMSNorm + SiLU, Wan VAE
     for C in (96, 192, 384):
         name = f"rmsnorm_silu_cl_wan_c{C}"

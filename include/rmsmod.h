@@ -213,17 +213,41 @@ int gated_rmsnorm_modulate(const void* residual, const void* update, const void*
  * qk_layernorm -- per-head LayerNorm with affine over head_dim values, q rows
  * and k rows in one launch, each tensor with its own weight and bias.
  *   [GLM] §Motivation (qk-norm nn.LayerNorm(128) on (1, S, 32, 128)) and
- *   §What "rounding-faithful" means here (q and k in one launch).
+ *   §What "rounding-faithful" means here (q and k in one launch; the same
+ *   kernel for head_dim <= 128 rows).
  *
  *     z[d] = R(((f(x[d]) - mean) * rstd) * f(w[d]) + f(b[d]))
- *   q, q_out [rows_q * head_dim]; k, k_out [rows_k * head_dim] (bf16);
- *   wq, bq, wk, bk bf16 [head_dim]; head_dim must be 128.
+ *   q, q_out [rows_q * head_dim]; k, k_out [rows_k * head_dim] (bf16, dense);
+ *   wq, bq, wk, bk bf16 [head_dim]; head_dim 64, 96 or 128.
  *   mean_out, rstd_out nullable fp32 [rows_q + rows_k], q rows first.
+ *   q_out may equal q and k_out may equal k (in place).
  * ---------------------------------------------------------------------- */
 int qk_layernorm(const void* q, const void* k, const void* wq, const void* bq, const void* wk,
                  const void* bk, void* q_out, void* k_out, int64_t rows_q, int64_t rows_k,
                  int64_t head_dim, float eps, float* mean_out, float* rstd_out,
                  rmsmod_stream_t stream);
+
+/* qk_layernorm_strided -- the same on token-strided views, such as the q and
+ * k slices of a fused QKV projection [tokens, 3, heads, head_dim].
+ *   [GLM] §What "rounding-faithful" means here (qk bullet) and the sites it
+ *   lists beyond (1, S, 32, 128).
+ *
+ *   Row (t, h) of q starts at q + t * q_token_stride + h * head_dim
+ *   (elements): the heads_q rows of a token are contiguous, tokens are
+ *   q_token_stride apart; likewise k (heads_k rows), q_out and k_out with
+ *   their own token strides.  Strides are multiples of 8 and at least
+ *   heads * head_dim (when tokens > 1).  Statistics rows are numbered
+ *   t * heads + h, q rows first.  q_out may equal q with the same stride (in
+ *   place, e.g. inside the QKV buffer); views that interleave in one buffer
+ *   without sharing bytes are accepted; any other overlap is
+ *   RMSMOD_ERR_UNSUPPORTED.  RMSMOD_ERR_STRIDE for a bad stride.
+ * ---------------------------------------------------------------------- */
+int qk_layernorm_strided(const void* q, const void* k, const void* wq, const void* bq,
+                         const void* wk, const void* bk, void* q_out, void* k_out,
+                         int64_t tokens, int64_t heads_q, int64_t heads_k, int64_t head_dim,
+                         int64_t q_token_stride, int64_t k_token_stride,
+                         int64_t q_out_token_stride, int64_t k_out_token_stride, float eps,
+                         float* mean_out, float* rstd_out, rmsmod_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * rmsnorm_silu_cl -- channels-last RMSNorm * gamma, then SiLU, with the

@@ -77,6 +77,7 @@ def library() -> ctypes.CDLL:
             "rmsnorm_modulate": [P, P, P, P, P, I, I, I, I, F, P, P],
             "gated_rmsnorm_modulate": [P, P, P, I, P, P, P, I, P, P, I, I, I, F, P, P],
             "qk_layernorm": [P, P, P, P, P, P, P, P, I, I, I, F, P, P, P],
+            "qk_layernorm_strided": [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, P, P],
             "rmsnorm_silu_cl": [P, P, C, P, P, I, I, F, P, P],
             "modulate_scale_shift": [P, P, P, P, I, I, I, I, P],
             "residual_gate_add": [P, P, P, I, P, I, I, I, P],
@@ -327,11 +328,32 @@ def gated_rmsnorm_modulate(residual, update, gate, weight, scale, shift, eps: fl
     return res_out, out
 
 
+def _token_view(t, name):
+    """[..., heads, head_dim] view with dense heads and one uniform stride
+    over the leading dims -> (tokens, heads, token_stride in elements)."""
+    _bf16(t, name)
+    if t.dim() < 2 or t.stride(-1) != 1 or (t.dim() >= 2 and t.shape[-2] > 1 and
+                                             t.stride(-2) != t.shape[-1]):
+        raise ValueError(f"{name}: heads must be dense [..., heads, head_dim]")
+    heads, hd = (t.shape[-2], t.shape[-1]) if t.dim() >= 2 else (1, t.shape[-1])
+    lead = list(zip(t.shape[:-2], t.stride()[:-2]))
+    tokens, ts = 1, heads * hd
+    for size, stride in reversed(lead):
+        if size == 1:
+            continue
+        if tokens == 1:
+            ts = stride
+        elif stride != ts * tokens:
+            raise ValueError(f"{name}: leading dims do not collapse to one token stride")
+        tokens *= size
+    return tokens, heads, ts
+
+
 def qk_layernorm(q, k, wq, bq, wk, bk, eps: float = 1e-5, q_out=None, k_out=None,
                  mean_out=None, rstd_out=None, stream=None):
-    """Per-head LayerNorm(head_dim) with affine on q and k in one launch. -> (q_out, k_out)."""
-    _dense(q, "q")
-    _dense(k, "k")
+    """Per-head LayerNorm(head_dim) with affine on q and k in one launch. -> (q_out, k_out).
+    q / k may be token-strided views (e.g. slices of a fused QKV projection)
+    whose heads are dense; head_dim 64, 96 or 128."""
     hd = q.shape[-1]
     if k.shape[-1] != hd:
         raise ValueError("q and k must share head_dim")
@@ -339,13 +361,38 @@ def qk_layernorm(q, k, wq, bq, wk, bk, eps: float = 1e-5, q_out=None, k_out=None
         _dense(t, n)
         if t.numel() != hd:
             raise ValueError(f"{n} must have head_dim elements")
-    rq, rk = q.numel() // hd, k.numel() // hd
-    q_out = _out_like(q_out, q, "q_out")
-    k_out = _out_like(k_out, k, "k_out")
-    _f32_out(mean_out, rq + rk, "mean_out", q.device)
-    _f32_out(rstd_out, rq + rk, "rstd_out", q.device)
-    _call("qk_layernorm", _ptr(q), _ptr(k), _ptr(wq), _ptr(bq), _ptr(wk), _ptr(bk), _ptr(q_out),
-          _ptr(k_out), rq, rk, hd, eps, _ptr(mean_out), _ptr(rstd_out), _stream(stream))
+    dense = all(t.is_contiguous() for t in (q, k)) and all(
+        t is None or t.is_contiguous() for t in (q_out, k_out))
+    if dense:
+        _dense(q, "q")
+        _dense(k, "k")
+        rq, rk = q.numel() // hd, k.numel() // hd
+        q_out = _out_like(q_out, q, "q_out")
+        k_out = _out_like(k_out, k, "k_out")
+        _f32_out(mean_out, rq + rk, "mean_out", q.device)
+        _f32_out(rstd_out, rq + rk, "rstd_out", q.device)
+        _call("qk_layernorm", _ptr(q), _ptr(k), _ptr(wq), _ptr(bq), _ptr(wk), _ptr(bk),
+              _ptr(q_out), _ptr(k_out), rq, rk, hd, eps, _ptr(mean_out), _ptr(rstd_out),
+              _stream(stream))
+        return q_out, k_out
+    tq, hq, qts = _token_view(q, "q")
+    tk, hk, kts = _token_view(k, "k")
+    if tq != tk:
+        raise ValueError("q and k must have the same number of tokens")
+    if q_out is None:
+        q_out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if k_out is None:
+        k_out = torch.empty(k.shape, dtype=k.dtype, device=k.device)
+    if q_out.shape != q.shape or k_out.shape != k.shape:
+        raise ValueError("q_out / k_out must match q / k")
+    to, _, qots = _token_view(q_out, "q_out")
+    _, _, kots = _token_view(k_out, "k_out")
+    rows = tq * (hq + hk)
+    _f32_out(mean_out, rows, "mean_out", q.device)
+    _f32_out(rstd_out, rows, "rstd_out", q.device)
+    _call("qk_layernorm_strided", _ptr(q), _ptr(k), _ptr(wq), _ptr(bq), _ptr(wk), _ptr(bk),
+          _ptr(q_out), _ptr(k_out), tq, hq, hk, hd, qts, kts, qots, kots, eps, _ptr(mean_out),
+          _ptr(rstd_out), _stream(stream))
     return q_out, k_out
 
 

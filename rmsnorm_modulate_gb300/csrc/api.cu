@@ -146,6 +146,8 @@ RMSMOD_EXPORT int rmsmod_device_status(unsigned int* bits, int clear)
     return RMSMOD_OK;
 }
 
+static bool qk_head_dim_ok(int64_t hd) { return hd == 64 || hd == 96 || hd == 128; }
+
 RMSMOD_EXPORT int rmsmod_supported(int op, int64_t D_or_C, const void* const* ptrs, int nptrs)
 {
     if (D_or_C <= 0 || D_or_C % 8 != 0)
@@ -159,7 +161,7 @@ RMSMOD_EXPORT int rmsmod_supported(int op, int64_t D_or_C, const void* const* pt
             return 0;
         break;
     case RMSMOD_OP_QK_LAYERNORM:
-        if (D_or_C != 128)
+        if (!qk_head_dim_ok(D_or_C))
             return 0;
         break;
     case RMSMOD_OP_RMSNORM_SILU_CL:
@@ -435,16 +437,36 @@ RMSMOD_EXPORT int gated_rmsnorm_modulate(const void* residual, const void* updat
     return launch_status(rmsmod::launch_row_kernel(rmsmod::kOpGated, a, dev, stream));
 }
 
-RMSMOD_EXPORT int qk_layernorm(const void* q, const void* k, const void* wq, const void* bq,
-                               const void* wk, const void* bk, void* q_out, void* k_out,
-                               int64_t rows_q, int64_t rows_k, int64_t head_dim, float eps,
-                               float* mean_out, float* rstd_out, rmsmod_stream_t stream)
+// Do two token-strided tensors (tokens rows of `len` bytes, `ts` bytes apart)
+// share a byte?  Same stride: compare the per-token windows modulo the
+// stride (q and k views of one fused QKV buffer interleave without
+// overlapping); otherwise compare the spans.
+static bool strided_overlap(const void* a, int64_t a_ts, int64_t a_len, const void* b,
+                            int64_t b_ts, int64_t b_len, int64_t tokens)
 {
-    if (rows_q < 0 || rows_k < 0 || head_dim != 128)
-        return RMSMOD_ERR_SHAPE;
-    if (tensor_bytes(rows_q, head_dim) < 0 || tensor_bytes(rows_k, head_dim) < 0 ||
-        rows_q > INT64_MAX / 2 - rows_k)
-        return RMSMOD_ERR_SHAPE;
+    if (!a || !b || tokens <= 0 || a_len <= 0 || b_len <= 0)
+        return false;
+    const int64_t a_span = (tokens - 1) * a_ts + a_len, b_span = (tokens - 1) * b_ts + b_len;
+    if (!overlap(a, a_span, b, b_span))
+        return false;
+    if (a_ts != b_ts || tokens == 1)
+        return true;
+    const int64_t ts = a_ts;
+    const int64_t diff = static_cast<int64_t>(reinterpret_cast<uintptr_t>(b) -
+                                              reinterpret_cast<uintptr_t>(a));
+    int64_t r = diff % ts;
+    if (r < 0)
+        r += ts;
+    return r < a_len || r + b_len > ts;
+}
+
+static int qk_launch(const void* q, const void* k, const void* wq, const void* bq,
+                     const void* wk, const void* bk, void* q_out, void* k_out, int64_t tokens,
+                     int64_t heads_q, int64_t heads_k, int64_t head_dim, int64_t q_ts,
+                     int64_t k_ts, int64_t qo_ts, int64_t ko_ts, float eps, float* mean_out,
+                     float* rstd_out, rmsmod_stream_t stream)
+{
+    const int64_t rows_q = tokens * heads_q, rows_k = tokens * heads_k;
     if (rows_q + rows_k == 0)
         return RMSMOD_OK;
     if ((rows_q > 0 && (!q || !wq || !bq || !q_out)) ||
@@ -454,34 +476,81 @@ RMSMOD_EXPORT int qk_layernorm(const void* q, const void* k, const void* wq, con
         !aligned(wk, 16) || !aligned(bk, 16) || !aligned(q_out, 16) || !aligned(k_out, 16) ||
         !aligned(mean_out, 4) || !aligned(rstd_out, 4))
         return RMSMOD_ERR_ALIGN;
-    const int64_t bq_bytes = tensor_bytes(rows_q, head_dim);
-    const int64_t bk_bytes = tensor_bytes(rows_k, head_dim);
+    // byte geometry of the four views: tokens rows of heads * head_dim values
+    const int64_t ql = 2 * heads_q * head_dim, kl = 2 * heads_k * head_dim;
+    const int64_t qts = 2 * q_ts, kts = 2 * k_ts, qots = 2 * qo_ts, kots = 2 * ko_ts;
     const int64_t nst = 4 * (rows_q + rows_k);
-    if (bad_alias(q_out, q, bq_bytes, true) || bad_alias(k_out, k, bk_bytes, true) ||
-        overlap(q_out, bq_bytes, k, bk_bytes) || overlap(k_out, bk_bytes, q, bq_bytes) ||
-        overlap(q_out, bq_bytes, k_out, bk_bytes) || overlap(mean_out, nst, rstd_out, nst) ||
-        overlap(q_out, bq_bytes, mean_out, nst) || overlap(k_out, bk_bytes, mean_out, nst) ||
-        overlap(q_out, bq_bytes, rstd_out, nst) || overlap(k_out, bk_bytes, rstd_out, nst))
+    const int64_t qo_span = rows_q ? (tokens - 1) * qots + ql : 0;
+    const int64_t ko_span = rows_k ? (tokens - 1) * kots + kl : 0;
+    // an output may be its own input exactly (same base, same stride)
+    const bool q_inplace = q_out == q && qo_ts == q_ts;
+    const bool k_inplace = k_out == k && ko_ts == k_ts;
+    if ((!q_inplace && strided_overlap(q_out, qots, ql, q, qts, ql, rows_q ? tokens : 0)) ||
+        (!k_inplace && strided_overlap(k_out, kots, kl, k, kts, kl, rows_k ? tokens : 0)) ||
+        strided_overlap(q_out, qots, ql, k, kts, kl, rows_q && rows_k ? tokens : 0) ||
+        strided_overlap(k_out, kots, kl, q, qts, ql, rows_q && rows_k ? tokens : 0) ||
+        strided_overlap(q_out, qots, ql, k_out, kots, kl, rows_q && rows_k ? tokens : 0) ||
+        overlap(mean_out, nst, rstd_out, nst) || overlap(q_out, qo_span, mean_out, nst) ||
+        overlap(k_out, ko_span, mean_out, nst) || overlap(q_out, qo_span, rstd_out, nst) ||
+        overlap(k_out, ko_span, rstd_out, nst))
         return RMSMOD_ERR_UNSUPPORTED;
     DeviceInfo dev;
     int st;
     if ((st = device_info(dev)) != RMSMOD_OK)
         return st;
     rmsmod::QkArgs a{};
-    a.q = q;
-    a.k = k;
-    a.wq = wq;
-    a.bq = bq;
-    a.wk = wk;
-    a.bk = bk;
-    a.q_out = q_out;
-    a.k_out = k_out;
+    a.t[0] = rmsmod::QkTensor{q, q_out, wq, bq, rows_q ? tokens : 0, heads_q, q_ts, qo_ts};
+    a.t[1] = rmsmod::QkTensor{k, k_out, wk, bk, rows_k ? tokens : 0, heads_k, k_ts, ko_ts};
     a.mean_out = mean_out;
     a.rstd_out = rstd_out;
-    a.rows_q = rows_q;
-    a.rows_k = rows_k;
+    a.head_dim = static_cast<int>(head_dim);
     a.eps = eps;
     return launch_status(rmsmod::launch_qk_kernel(a, dev, stream));
+}
+
+RMSMOD_EXPORT int qk_layernorm(const void* q, const void* k, const void* wq, const void* bq,
+                               const void* wk, const void* bk, void* q_out, void* k_out,
+                               int64_t rows_q, int64_t rows_k, int64_t head_dim, float eps,
+                               float* mean_out, float* rstd_out, rmsmod_stream_t stream)
+{
+    if (rows_q < 0 || rows_k < 0 || !qk_head_dim_ok(head_dim))
+        return RMSMOD_ERR_SHAPE;
+    if (tensor_bytes(rows_q, head_dim) < 0 || tensor_bytes(rows_k, head_dim) < 0 ||
+        rows_q > INT64_MAX / 2 - rows_k)
+        return RMSMOD_ERR_SHAPE;
+    // a dense tensor is one "token" of rows heads
+    if (rows_q + rows_k == 0)
+        return RMSMOD_OK;
+    return qk_launch(q, k, wq, bq, wk, bk, q_out, k_out, 1, rows_q, rows_k, head_dim,
+                     rows_q * head_dim, rows_k * head_dim, rows_q * head_dim,
+                     rows_k * head_dim, eps, mean_out, rstd_out, stream);
+}
+
+RMSMOD_EXPORT int qk_layernorm_strided(const void* q, const void* k, const void* wq,
+                                       const void* bq, const void* wk, const void* bk,
+                                       void* q_out, void* k_out, int64_t tokens,
+                                       int64_t heads_q, int64_t heads_k, int64_t head_dim,
+                                       int64_t q_token_stride, int64_t k_token_stride,
+                                       int64_t q_out_token_stride, int64_t k_out_token_stride,
+                                       float eps, float* mean_out, float* rstd_out,
+                                       rmsmod_stream_t stream)
+{
+    if (tokens < 0 || heads_q < 0 || heads_k < 0 || !qk_head_dim_ok(head_dim))
+        return RMSMOD_ERR_SHAPE;
+    if (tokens > 0 && (heads_q > INT64_MAX / head_dim / tokens / 2 ||
+                       heads_k > INT64_MAX / head_dim / tokens / 2))
+        return RMSMOD_ERR_SHAPE;
+    const int64_t strides[4] = {q_token_stride, k_token_stride, q_out_token_stride,
+                                k_out_token_stride};
+    const int64_t need[4] = {heads_q * head_dim, heads_k * head_dim, heads_q * head_dim,
+                             heads_k * head_dim};
+    for (int i = 0; i < 4; ++i)
+        if (need[i] > 0 && tokens > 1 &&
+            (strides[i] < need[i] || strides[i] % 8 != 0 || strides[i] > INT64_MAX / 4 / tokens))
+            return RMSMOD_ERR_STRIDE;
+    return qk_launch(q, k, wq, bq, wk, bk, q_out, k_out, tokens, heads_q, heads_k, head_dim,
+                     q_token_stride, k_token_stride, q_out_token_stride, k_out_token_stride, eps,
+                     mean_out, rstd_out, stream);
 }
 
 RMSMOD_EXPORT int rmsnorm_silu_cl(const void* x, const void* bias, int bias_is_fp32,

@@ -88,19 +88,26 @@ struct RowArgs {
 cudaError_t launch_row_kernel(int op, const RowArgs& a, const DeviceInfo& dev,
                               cudaStream_t stream);
 
+// One of the two tensors of a qk launch: rows = tokens * heads head rows of
+// head_dim values; the heads of a token are contiguous, tokens are in_ts /
+// out_ts elements apart (a strided view of a fused QKV projection, or
+// tokens = 1 for a dense tensor).
+struct QkTensor {
+    const void* in;
+    void* out;
+    const void* w;
+    const void* b;
+    int64_t tokens;
+    int64_t heads;
+    int64_t in_ts;   // elements, a multiple of 8
+    int64_t out_ts;
+};
+
 struct QkArgs {
-    const void* q;
-    const void* k;
-    const void* wq;
-    const void* bq;
-    const void* wk;
-    const void* bk;
-    void* q_out;
-    void* k_out;
-    float* mean_out;
+    QkTensor t[2];     // q, k
+    float* mean_out;   // nullable [rows_q + rows_k], q rows first
     float* rstd_out;
-    int64_t rows_q;
-    int64_t rows_k;
+    int head_dim;      // 64, 96 or 128
     float eps;
 };
 

@@ -1,18 +1,21 @@
-// qk_layernorm on sm_103a: per-head LayerNorm(128) with affine, q rows and k
-// rows in one launch (sglang #34008 GLM-Image, §Motivation qk-norm bullet and
-// §What "rounding-faithful" means here, qk bullet).
+// qk_layernorm on sm_103a: per-head LayerNorm(head_dim) with affine, q rows
+// and k rows in one launch (sglang #34008 GLM-Image, §Motivation qk-norm
+// bullet and §What "rounding-faithful" means here, qk bullet; head_dim 64 /
+// 96 and strided q/k views of a fused QKV projection at the other sites the
+// page lists).
 //
-// A 128-element head row is 256 bytes (16 vectors of eight bf16).  P lanes
-// own one row (16 / P vectors each), so a warp covers a tile of 32 / P
-// consecutive rows per step and every lane is busy -- the eager kernel
-// spends a 128-thread block per row with three of its four warps idle.
-// Tiles reach shared memory by 1-D bulk copies (TMA) into a ring per warp,
-// so the next tiles are in flight while one is computed.  Blocks are split
-// between the q rows and the k rows in proportion; a block stages its
-// weight and bias once, widened to fp32, in shared memory.  A lane visits
-// its vectors in an order rotated by its row inside the tile, which keeps
-// the row reads (256-byte stride) and the weight reads free of bank
-// conflicts.
+// A head row of head_dim = 8 * RV values is RV 16-byte vectors.  P lanes own
+// one row (V = RV / P vectors each), so a warp covers a tile of 32 / P rows
+// per step and every lane is busy -- the eager kernel spends a 128-thread
+// block per row with three of its four warps idle.  The rows of a tile are
+// consecutive heads of one token, so a tile is one contiguous span even when
+// q and k are token-strided views; tiles reach shared memory by 1-D bulk
+// copies (TMA) into a ring per warp, so the next tiles are in flight while
+// one is computed.  Blocks are split between the q rows and the k rows in
+// proportion; a block stages its weight and bias once, widened to fp32, in
+// shared memory.  A lane visits its vectors in an order rotated by its row
+// inside the tile, which keeps the row reads and the weight reads free of
+// bank conflicts at 64 and 128 values per row (two-way at 96).
 //
 //   z = R(((x - mean) * rstd) * w + b)   -- fp32, one final rounding
 #include "device_common.cuh"
@@ -26,39 +29,74 @@ __device__ unsigned int g_error;
 
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kRowVec = 16;                       // 16-byte vectors per row
-constexpr int kLanesPerRow = 2;                   // P
-constexpr int kVecPerLane = kRowVec / kLanesPerRow;
-constexpr int kTileRows = 32 / kLanesPerRow;      // rows per warp step
-constexpr int kTileVec = kTileRows * kRowVec;     // 16-byte vectors per tile
 constexpr int kStages = 3;
-constexpr int kSmem = kWarps * kStages * kTileVec * 16;
-constexpr int kL = 6;                             // 8 * kVecPerLane = 2^kL values per lane
-static_assert((8 << kL) == 8 * 8 * kVecPerLane, "kL must be log2 of the values per lane");
+constexpr int kMaxRowVec = 16;  // head_dim <= 128
 
+template <int N>
+struct Log2Ceil {
+    static constexpr int value = (N <= 1) ? 0 : 1 + Log2Ceil<(N + 1) / 2>::value;
+};
+template <>
+struct Log2Ceil<1> {
+    static constexpr int value = 0;
+};
+
+template <int RV, int P>
+struct QkShape {
+    static constexpr int kVecPerLane = RV / P;
+    static constexpr int kTileRows = 32 / P;
+    static constexpr int kTileVec = kTileRows * RV;
+    static constexpr int kSmem = kWarps * kStages * kTileVec * 16;
+    static constexpr int kL = Log2Ceil<8 * kVecPerLane>::value;
+    static_assert(RV % P == 0, "a lane owns whole vectors");
+};
+
+template <int RV, int P>
 __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blocks_q)
 {
     grid_dependency_sync();
+    using Shape = QkShape<RV, P>;
+    constexpr int V = Shape::kVecPerLane;
+    constexpr int kTileRows = Shape::kTileRows;
+    constexpr int kTileVec = Shape::kTileVec;
+    constexpr int kL = Shape::kL;
+    constexpr float kN = 8.0f * RV;
+
     extern __shared__ __align__(128) uint4 ring[];
     __shared__ __align__(8) unsigned long long bars[kWarps][kStages];
-    // weight and bias of this block's tensor, fp32, as [vector][half] float4
-    __shared__ __align__(16) float4 s_w[2][kRowVec], s_b[2][kRowVec];
+    // weight and bias of this block's tensor, fp32, as [half][vector] float4
+    __shared__ __align__(16) float4 s_w[2][kMaxRowVec], s_b[2][kMaxRowVec];
 
     const bool is_q = static_cast<int>(blockIdx.x) < blocks_q;
-    const int64_t rows = is_q ? a.rows_q : a.rows_k;
+    const QkTensor t = is_q ? a.t[0] : a.t[1];
     const int blk = is_q ? blockIdx.x : blockIdx.x - blocks_q;
     const int nblk = is_q ? blocks_q : gridDim.x - blocks_q;
-    const uint4* __restrict__ src = static_cast<const uint4*>(is_q ? a.q : a.k);
-    uint4* __restrict__ dst = static_cast<uint4*>(is_q ? a.q_out : a.k_out);
-    const uint4* __restrict__ wv = static_cast<const uint4*>(is_q ? a.wq : a.wk);
-    const uint4* __restrict__ bv = static_cast<const uint4*>(is_q ? a.bq : a.bk);
-    const int64_t stat_off = is_q ? 0 : a.rows_q;
+    const uint4* __restrict__ src = static_cast<const uint4*>(t.in);
+    uint4* __restrict__ dst = static_cast<uint4*>(t.out);
+    const uint4* __restrict__ wv = static_cast<const uint4*>(t.w);
+    const uint4* __restrict__ bv = static_cast<const uint4*>(t.b);
+    const int64_t stat_off = is_q ? 0 : a.t[0].tokens * a.t[0].heads;
+    // tiles: (token, chunk of kTileRows consecutive heads)
+    const int64_t chunks = (t.heads + kTileRows - 1) / kTileRows;
+    const int64_t tiles = t.tokens * chunks;
+    const int64_t in_tv = t.in_ts / 8, out_tv = t.out_ts / 8;  // token strides, vectors
+    // tile -> token: none for a dense tensor (one token), 32-bit division
+    // whenever the tile count allows
+    const bool one_token = t.tokens == 1;
+    const bool small = tiles < (int64_t(1) << 32);
+    auto token_of = [&](int64_t tile) -> int64_t {
+        if (one_token)
+            return 0;
+        if (small)
+            return static_cast<uint32_t>(tile) / static_cast<uint32_t>(chunks);
+        return tile / chunks;
+    };
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int sub = lane % kLanesPerRow;   // position inside the row
-    const int rsub = lane / kLanesPerRow;  // row inside the tile
-    const int rot = rsub % kVecPerLane;
+    const int sub = lane % P;   // position inside the row
+    const int rsub = lane / P;  // row inside the tile
+    const int rot = rsub % V;
 
     uint4* wbuf = ring + warp * kStages * kTileVec;
     const uint32_t bar0 = smem_addr(&bars[warp][0]);
@@ -73,22 +111,25 @@ __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blo
     const int64_t first = static_cast<int64_t>(blk) * kWarps + warp;  // tile index
     const int64_t step = static_cast<int64_t>(nblk) * kWarps;
     auto issue = [&](int64_t k) {
-        const int64_t row0 = (first + k * step) * kTileRows;
-        if (lane != 0 || row0 >= rows)
+        const int64_t tile = first + k * step;
+        if (lane != 0 || tile >= tiles)
             return;
-        const int64_t left = rows - row0;
-        const uint32_t bytes = static_cast<uint32_t>(left < kTileRows ? left : kTileRows) * 256u;
+        const int64_t tok = token_of(tile);
+        const int64_t h0 = (tile - tok * chunks) * kTileRows;
+        const int64_t left = t.heads - h0;
+        const uint32_t bytes =
+            static_cast<uint32_t>(left < kTileRows ? left : kTileRows) * (RV * 16u);
         const int st = static_cast<int>(k % kStages);
         const uint32_t bar = bar0 + 8u * st;
         fence_proxy_async();
         mbar_expect_tx(bar, bytes);
-        bulk_g2s(smem_addr(wbuf + st * kTileVec), src + row0 * kRowVec, bytes, bar);
+        bulk_g2s(smem_addr(wbuf + st * kTileVec), src + tok * in_tv + h0 * RV, bytes, bar);
     };
 #pragma unroll
     for (int k = 0; k < kStages; ++k)
         issue(k);
 
-    if (threadIdx.x < 2 * kRowVec) {
+    if (threadIdx.x < 2 * RV) {
         const int c = threadIdx.x >> 1, h = threadIdx.x & 1;
         const uint4 w = ld_cached(wv + c), b = ld_cached(bv + c);
         const uint32_t w0 = h ? w.z : w.x, w1 = h ? w.w : w.y;
@@ -103,10 +144,12 @@ __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blo
     }
     __syncthreads();
 
-    const float n = 128.0f, inv_n = 1.0f / 128.0f;
+    const float inv_n = 1.0f / kN;
     bool broken = false;
-    for (int64_t k = 0; (first + k * step) * kTileRows < rows; ++k) {
-        const int64_t row0 = (first + k * step) * kTileRows;
+    for (int64_t k = 0; first + k * step < tiles; ++k) {
+        const int64_t tile = first + k * step;
+        const int64_t tok = token_of(tile);
+        const int64_t h0 = (tile - tok * chunks) * kTileRows;
         const int st = static_cast<int>(k % kStages);
         if (!broken && !mbar_wait(bar0 + 8u * st, static_cast<uint32_t>((k / kStages) & 1),
                                   kWaitLimitNs)) {
@@ -114,40 +157,44 @@ __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blo
             if (lane == 0)
                 atomicOr(&g_error, kErrCopyTimeout);
         }
-        const int64_t row = row0 + rsub;
-        const bool valid = row < rows;
-        const int64_t base = row * kRowVec;
+        const int64_t h = h0 + rsub;
+        const bool valid = h < t.heads;
+        const int64_t row = tok * t.heads + h;  // dense row number, for the statistics
+        const int64_t base = tok * out_tv + h * RV;
 
         // vector j of this lane is c(j) = sub + P * ((j + rot) mod V)
-        const uint4* tile = wbuf + st * kTileVec + rsub * kRowVec;
-        uint4 xv[kVecPerLane];
+        const uint4* tile_p = wbuf + st * kTileVec + rsub * RV;
+        uint4 xv[V];
 #pragma unroll
-        for (int j = 0; j < kVecPerLane; ++j) {
-            const int jj = (j + rot) % kVecPerLane;
-            xv[j] = valid ? tile[sub + kLanesPerRow * jj] : make_uint4(0u, 0u, 0u, 0u);
+        for (int j = 0; j < V; ++j) {
+            const int jj = (j + rot) % V;
+            xv[j] = valid ? tile_p[sub + P * jj] : make_uint4(0u, 0u, 0u, 0u);
         }
         __syncwarp();
         issue(k + kStages);
 
-        const uint32_t mm = tree_absmax<kVecPerLane>(xv);
+        const uint32_t mm = tree_absmax<V>(xv);
         ExactSums<true> acc;
         const uint32_t E = offset_exponent(mm);
         acc.init(offset_k1<kL>(E), offset_k2<kL>(E));
 #pragma unroll
-        for (int j = 0; j < kVecPerLane; ++j)
+        for (int j = 0; j < V; ++j)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 acc.add(f2_from_bf2(word(xv[j], i)));
         float s1h, s1l, s2h, s2l;
         acc.lane_total(s1h, s1l, s2h, s2l);
-        dd2_allreduce<kLanesPerRow>(s1h, s1l, s2h, s2l);
+        dd2_allreduce<P>(s1h, s1l, s2h, s2l);
 
         // row class over its lanes
-        uint32_t cls = allreduce_max<kLanesPerRow>(static_cast<uint32_t>(magnitude_class(mm)));
-        uint32_t emax = allreduce_max<kLanesPerRow>(mm == 0 ? 0u : (mm >> 7));
+        uint32_t cls = allreduce_max<P>(static_cast<uint32_t>(magnitude_class(mm)));
+        uint32_t emax = allreduce_max<P>(mm == 0 ? 0u : (mm >> 7));
 
         float mean, var;
-        finalize_ln_pow2(s1h, s1l, s2h, s2l, n, inv_n, mean, var);
+        if ((RV & (RV - 1)) == 0)
+            finalize_ln_pow2(s1h, s1l, s2h, s2l, kN, inv_n, mean, var);
+        else
+            finalize_ln(s1h, s1l, s2h, s2l, kN, inv_n, mean, var);
         if (__any_sync(kFullMask, cls != kClassFast)) {
             // Rare: some row of this tile holds Inf/NaN or extreme magnitudes.
             // Every lane runs both slow variants (warp-uniform control flow)
@@ -158,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blo
             ExactSums<true> acc2;
             acc2.init(offset_k1<kL>(127u), offset_k2<kL>(127u));
 #pragma unroll
-            for (int j = 0; j < kVecPerLane; ++j)
+            for (int j = 0; j < V; ++j)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const u64 xx = f2_from_bf2(word(xv[j], i));
@@ -168,17 +215,20 @@ __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blo
                     p2 = __fadd_rn(__fadd_rn(p2, __fmul_rn(lo, lo)), __fmul_rn(hi, hi));
                     acc2.add(rs.apply(xx));
                 }
-            p1 = allreduce_add<kLanesPerRow>(p1);
-            p2 = allreduce_add<kLanesPerRow>(p2);
+            p1 = allreduce_add<P>(p1);
+            p2 = allreduce_add<P>(p2);
             float t1h, t1l, t2h, t2l;
             acc2.lane_total(t1h, t1l, t2h, t2l);
-            dd2_allreduce<kLanesPerRow>(t1h, t1l, t2h, t2l);
+            dd2_allreduce<P>(t1h, t1l, t2h, t2l);
             if (cls == kClassNonFinite) {
                 mean = __fmul_rn(p1, inv_n);
                 var = __fsub_rn(__fmul_rn(p2, inv_n), __fmul_rn(mean, mean));
             } else if (cls == kClassScaled) {
                 float ms, vs;
-                finalize_ln_pow2(t1h, t1l, t2h, t2l, n, inv_n, ms, vs);
+                if ((RV & (RV - 1)) == 0)
+                    finalize_ln_pow2(t1h, t1l, t2h, t2l, kN, inv_n, ms, vs);
+                else
+                    finalize_ln(t1h, t1l, t2h, t2l, kN, inv_n, ms, vs);
                 mean = rs.unscale(ms, 1);
                 var = rs.unscale(vs, 2);
             }
@@ -193,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blo
         if (valid) {
             const u64 mean2 = f2_splat(mean), rstd2 = f2_splat(rstd);
 #pragma unroll
-            for (int j = 0; j < kVecPerLane; ++j) {
-                const int c = sub + kLanesPerRow * ((j + rot) % kVecPerLane);
+            for (int j = 0; j < V; ++j) {
+                const int c = sub + P * ((j + rot) % V);
                 const float4 w_lo = s_w[0][c], w_hi = s_w[1][c];
                 const float4 b_lo = s_b[0][c], b_hi = s_b[1][c];
                 const u64 w2[4] = {f2_pack(w_lo.x, w_lo.y), f2_pack(w_lo.z, w_lo.w),
@@ -216,42 +266,61 @@ __global__ void __launch_bounds__(kThreads, 2) qk_kernel(const QkArgs a, int blo
         drain_pause();
 }
 
-}  // namespace
-
-cudaError_t launch_qk_kernel(const QkArgs& a, const DeviceInfo& dev, cudaStream_t stream)
+template <int RV, int P>
+cudaError_t launch_shape(const QkArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
+    using Shape = QkShape<RV, P>;
+    auto kern = qk_kernel<RV, P>;
     static int blocks_per_sm[64] = {0};
     const int d = dev.device & 63;
     if (blocks_per_sm[d] == 0) {
         cudaError_t e =
-            cudaFuncSetAttribute(qk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Shape::kSmem);
         if (e != cudaSuccess)
             return e;
         int nb = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, qk_kernel, kThreads, kSmem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads, Shape::kSmem);
         if (e != cudaSuccess)
             return e;
         blocks_per_sm[d] = nb > 0 ? nb : 1;
     }
-    constexpr int kRowsPerBlock = kTileRows * kWarps;
-    const int64_t total = a.rows_q + a.rows_k;
+    auto tiles_of = [](const QkTensor& t) {
+        return t.tokens * ((t.heads + Shape::kTileRows - 1) / Shape::kTileRows);
+    };
+    const int64_t tq = tiles_of(a.t[0]), tk = tiles_of(a.t[1]);
+    const int64_t total = tq + tk;
     const int64_t cap = static_cast<int64_t>(dev.sms) * blocks_per_sm[d];
-    const int64_t need_q = (a.rows_q + kRowsPerBlock - 1) / kRowsPerBlock;
-    const int64_t need_k = (a.rows_k + kRowsPerBlock - 1) / kRowsPerBlock;
+    const int64_t need_q = (tq + kWarps - 1) / kWarps;
+    const int64_t need_k = (tk + kWarps - 1) / kWarps;
     int64_t bq, bk;
     if (need_q + need_k <= cap) {
         bq = need_q;
         bk = need_k;
     } else {
-        bq = (cap * a.rows_q + total / 2) / total;
-        if (a.rows_q > 0 && bq < 1)
+        bq = (cap * tq + total / 2) / total;
+        if (tq > 0 && bq < 1)
             bq = 1;
-        if (a.rows_k > 0 && cap - bq < 1)
+        if (tk > 0 && cap - bq < 1)
             bq = cap - 1;
         bk = cap - bq;
     }
     const int grid = static_cast<int>(bq + bk);
-    return launch_dependent(qk_kernel, grid, kThreads, kSmem, stream, a, static_cast<int>(bq));
+    return launch_dependent(kern, grid, kThreads, Shape::kSmem, stream, a, static_cast<int>(bq));
+}
+
+}  // namespace
+
+// head_dim 64: one lane per row (8 vectors); 96 and 128: two lanes per row.
+cudaError_t launch_qk_kernel(const QkArgs& a, const DeviceInfo& dev, cudaStream_t stream)
+{
+    switch (a.head_dim) {
+    case 64:
+        return launch_shape<8, 1>(a, dev, stream);
+    case 96:
+        return launch_shape<12, 2>(a, dev, stream);
+    default:
+        return launch_shape<16, 2>(a, dev, stream);
+    }
 }
 
 cudaError_t qk_kernel_error(unsigned* bits, bool clear)

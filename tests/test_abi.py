@@ -176,14 +176,40 @@ def test_rms_and_gated_validation(lib):
     assert g(*bad) == ERR_UNSUPPORTED
 
 
+def test_qk_strided_validation(lib):
+    f = lib.qk_layernorm_strided
+    I = ctypes.c_int64
+    f.argtypes = [P] * 8 + [I] * 8 + [ctypes.c_float, P, P, P]
+    s = P(0)
+    T, H, hd = 16, 4, 128
+    qkv = A                     # [T, 3, H, hd] bf16: token stride 3 * H * hd
+    ts = 3 * H * hd
+    q, k = qkv, qkv + 2 * H * hd
+    w = A + (1 << 26)
+    args = lambda **kw: [p(kw.get("q", q)), p(kw.get("k", k)), p(w), p(w + 256), p(w + 512),
+                         p(w + 768), p(kw.get("qo", A + (1 << 27))),
+                         p(kw.get("ko", A + (1 << 28))), kw.get("T", T), kw.get("hq", H),
+                         kw.get("hk", H), kw.get("hd", hd), kw.get("qts", ts), kw.get("kts", ts),
+                         kw.get("qots", H * hd), kw.get("kots", H * hd), 1e-5, None, None, s]
+    assert f(*args(hd=80)) == ERR_SHAPE
+    assert f(*args(qts=H * hd - 8)) == ERR_STRIDE       # shorter than a token's heads
+    assert f(*args(kts=ts + 4)) == ERR_STRIDE           # not a multiple of 8
+    # q_out = the k slice of the same buffer while k is read: shared bytes
+    assert f(*args(qo=k, qots=ts)) == ERR_UNSUPPORTED
+    # a dense q_out that overlaps the strided q span partially
+    assert f(*args(qo=q + 2 * hd, qots=H * hd)) == ERR_UNSUPPORTED
+    assert f(*args(T=0)) == OK                           # nothing to do
+
+
 def test_qk_validation(lib):
     s = P(0)
     f = lib.qk_layernorm
     base = [p(A), p(A + 1 << 20), p(A + 1 << 21), p(A + 1 << 22), p(A + 1 << 23), p(A + 1 << 24),
             p(A + 1 << 25), p(A + 1 << 26), 4, 4, 128, 1e-5, None, None, s]
-    bad = list(base)
-    bad[10] = 64
-    assert f(*bad) == ERR_SHAPE
+    for hd in (32, 80, 100, 256):  # head_dim 64, 96, 128 only
+        bad = list(base)
+        bad[10] = hd
+        assert f(*bad) == ERR_SHAPE
     bad = list(base)
     bad[8] = -1
     assert f(*bad) == ERR_SHAPE
@@ -223,7 +249,9 @@ def test_supported_predicate(lib):
     assert lib.rmsmod_supported(1, 3073, arr, 3) == 0
     assert lib.rmsmod_supported(1, 16392, arr, 3) == 0
     assert lib.rmsmod_supported(4, 128, arr, 3) == 1
-    assert lib.rmsmod_supported(4, 64, arr, 3) == 0
+    assert lib.rmsmod_supported(4, 64, arr, 3) == 1
+    assert lib.rmsmod_supported(4, 96, arr, 3) == 1
+    assert lib.rmsmod_supported(4, 80, arr, 3) == 0
     assert lib.rmsmod_supported(5, 96, arr, 3) == 1
     assert lib.rmsmod_supported(5, 2048, arr, 3) == 0
     assert lib.rmsmod_supported(99, 96, arr, 3) == 0

@@ -130,8 +130,9 @@ def test_rms_normalize_brute_force(oracle_mod, D, with_w):
         assert np.allclose(rms_y, np.sqrt(ms / (ms + eps))[:, 0], rtol=2.0 ** -8)
 
 
-def test_qk_brute_force_and_library(oracle_mod):
-    inp = W.qk_inputs(300, 200, 128, seed=1)
+@pytest.mark.parametrize("hd", [128, 96, 64])
+def test_qk_brute_force_and_library(oracle_mod, hd):
+    inp = W.qk_inputs(300, 200, hd, seed=1)
     eps = 1e-5
     qo, ko, mean, rstd = oracle_mod.qk_layernorm(inp["q"], inp["k"], inp["wq"], inp["bq"],
                                                  inp["wk"], inp["bk"], eps)
@@ -147,7 +148,7 @@ def test_qk_brute_force_and_library(oracle_mod):
         near = dist <= bound
         assert np.array_equal(o[~near], r[~near])
         assert near.mean() < 1e-3
-        ref = torch.nn.functional.layer_norm(torch.from_numpy(xf), (128,),
+        ref = torch.nn.functional.layer_norm(torch.from_numpy(xf), (hd,),
                                              torch.from_numpy(widen(w).astype(np.float64)),
                                              torch.from_numpy(widen(b).astype(np.float64)),
                                              eps).numpy()

@@ -106,6 +106,13 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// One plain arrival (release semantics: this thread's earlier shared-memory
+// writes are visible to threads that observe the phase complete).
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // Makes barrier initialisation visible to the asynchronous (TMA) proxy.
 __device__ __forceinline__ void mbar_init_fence()
 {

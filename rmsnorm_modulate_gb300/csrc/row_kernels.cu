@@ -455,6 +455,313 @@ __global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads, RowShape<OP, V
         drain_pause();
 }
 
+// ---------------------------------------------------------------------------
+// Warp-specialised variant for one warp per row (LN / RMS / folded LN,
+// 2048 < D <= 3072).  The CTA owns a ring of kSlots row buffers fed by 1-D
+// bulk copies.  Statistics warps take rows in turn and stream them from
+// shared memory (abs-max, exact sums, butterfly, finalisation, rstd), leave
+// mean / rstd beside the row and arrive on the slot's "ready" barrier;
+// output warps wait for it, normalise + modulate the row from the same
+// buffer, store it, and refill the slot with the row kSlots ahead.  The
+// latency-bound reductions of some rows thus overlap the FMA-bound epilogue
+// of others instead of running in lock-step phases.
+// ---------------------------------------------------------------------------
+
+template <int OP, int V>
+struct WsShape {
+    static constexpr int kStatWarps = 8;
+    static constexpr int kOutWarps = 4;
+    static constexpr int kWarps = kStatWarps + kOutWarps;
+    static constexpr int kThreads = 32 * kWarps;
+    static constexpr int kSegVec = 32 * V;
+    static constexpr int kNmod = (OP == kOpLN || OP == kOpLNFold) ? 2 : 3;
+    static constexpr int kCacheBytes = kNmod * 32 * V * 16;
+    // Rows r and r + kSlots share a slot; with kSlots a multiple of both warp
+    // counts they also share their statistics warp and their output warp,
+    // which take their rows in order, so no barrier is ever waited on with
+    // the parity of a phase two steps ahead (which would read as complete).
+    static constexpr int kSlotsRaw = (100 * 1024) / (kSegVec * 16);
+    static constexpr int kSlots = kSlotsRaw / kStatWarps * kStatWarps;
+    static constexpr int kRingBytes = kSlots * kSegVec * 16;
+    static_assert(kSlots >= kStatWarps && kSlots % kStatWarps == 0 && kSlots % kOutWarps == 0,
+                  "a slot must return to the same statistics and output warps");
+};
+
+// Statistics of a non-fast row (see slow_stats) streamed from its buffer.
+template <bool kNeedSum, int V, int kL, bool EXACT>
+__device__ __noinline__ void slow_stats_smem(const uint4* buf, int Dv, uint32_t cls,
+                                             uint32_t emax, int lane, float n, float inv_n,
+                                             float& mean, float& stat)
+{
+    if (cls == kClassNonFinite) {
+        float p1 = 0.0f, p2 = 0.0f;
+        for (int j = 0; j < V; ++j) {
+            const int v = j * 32 + lane;
+            const uint4 xv = (EXACT || v < Dv) ? buf[v] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float lo, hi;
+                f2_unpack(f2_from_bf2(word(xv, i)), lo, hi);
+                p1 = __fadd_rn(__fadd_rn(p1, lo), hi);
+                p2 = __fadd_rn(__fadd_rn(p2, __fmul_rn(lo, lo)), __fmul_rn(hi, hi));
+            }
+        }
+        p1 = allreduce_add<32>(p1);
+        p2 = allreduce_add<32>(p2);
+        mean = __fmul_rn(p1, inv_n);
+        const float msq = __fmul_rn(p2, inv_n);
+        stat = kNeedSum ? __fsub_rn(msq, __fmul_rn(mean, mean)) : msq;
+        return;
+    }
+    RowScale rs;
+    rs.set(emax);
+    ExactSums<kNeedSum> acc;
+    acc.init(offset_k1<kL>(127u), offset_k2<kL>(127u));
+    for (int j = 0; j < V; ++j) {
+        const int v = j * 32 + lane;
+        const uint4 xv = (EXACT || v < Dv) ? buf[v] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            acc.add(rs.apply(f2_from_bf2(word(xv, i))));
+    }
+    float s1h, s1l, s2h, s2l;
+    acc.lane_total(s1h, s1l, s2h, s2l);
+    if (kNeedSum) {
+        dd2_allreduce<32>(s1h, s1l, s2h, s2l);
+        float ms, vs;
+        finalize_ln(s1h, s1l, s2h, s2l, n, inv_n, ms, vs);
+        mean = rs.unscale(ms, 1);
+        stat = rs.unscale(vs, 2);
+    } else {
+        dd_allreduce<32>(s2h, s2l);
+        mean = 0.0f;
+        stat = rs.unscale(finalize_ms(s2h, s2l, n, inv_n), 2);
+    }
+}
+
+template <int OP, int V, bool EXACT>
+__global__ void __launch_bounds__(WsShape<OP, V>::kThreads, 2)
+    row_kernel_ws(const RowArgs a, const Items items)
+{
+    grid_dependency_sync();
+    using Shape = WsShape<OP, V>;
+    constexpr int kSlots = Shape::kSlots;
+    constexpr int kSegVec = Shape::kSegVec;
+    constexpr int kStatWarps = Shape::kStatWarps;
+    constexpr int kOutWarps = Shape::kOutWarps;
+    constexpr int kL = Log2Ceil<8 * V>::value;
+    constexpr bool kNeedSum = (OP == kOpLN || OP == kOpLNFold);
+    constexpr bool kWeighted = (OP == kOpRMS);
+    static_assert(OP != kOpGated, "the gated op keeps the register-ring kernel");
+
+    extern __shared__ __align__(128) uint4 ring[];
+    __shared__ __align__(8) unsigned long long full_bar[kSlots], ready_bar[kSlots];
+    __shared__ float2 slot_stats[kSlots];  // (mean, rstd) of the row in each slot
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int Dv = a.Dv;
+    const uint32_t row_bytes = static_cast<uint32_t>(Dv) * 16u;
+
+    const uint4* __restrict__ src = static_cast<const uint4*>(a.x);
+    const uint4* __restrict__ weight = static_cast<const uint4*>(a.weight);
+    const uint4* __restrict__ scale = static_cast<const uint4*>(a.scale);
+    const uint4* __restrict__ shift = static_cast<const uint4*>(a.shift);
+    uint4* __restrict__ out = static_cast<uint4*>(a.out);
+    const bool has_w = (weight != nullptr);
+
+    uint4* cache = ring + Shape::kRingBytes / 16;
+    uint4* c_s1 = cache;
+    uint4* c_sh = cache + Dv;
+    uint4* c_w = cache + 2 * Dv;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(smem_addr(&full_bar[s]), 1u);
+            mbar_init(smem_addr(&ready_bar[s]), 1u);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    bool broken = false;
+    int64_t uses = 0;  // rows the CTA has run through its ring
+
+    for (int64_t item = blockIdx.x; item < items.count; item += gridDim.x) {
+        const int64_t b = item / items.per_batch;
+        const int64_t r_begin = b * a.S + (item % items.per_batch) * items.chunk;
+        const int64_t r_lim = (b + 1) * a.S;
+        const int64_t r_end = r_begin + items.chunk < r_lim ? r_begin + items.chunk : r_lim;
+        const int64_t nrows = r_end > r_begin ? r_end - r_begin : 0;
+
+        auto slot_of = [&](int64_t r) { return static_cast<int>((uses + r) % kSlots); };
+        auto parity_of = [&](int64_t r) {
+            return static_cast<uint32_t>(((uses + r) / kSlots) & 1);
+        };
+        auto issue = [&](int64_t r) {  // one thread
+            if (r >= nrows)
+                return;
+            const int s = slot_of(r);
+            const uint32_t bar = smem_addr(&full_bar[s]);
+            fence_proxy_async();
+            mbar_expect_tx(bar, row_bytes);
+            bulk_g2s(smem_addr(ring + s * kSegVec), src + (r_begin + r) * Dv, row_bytes, bar);
+        };
+        auto wait = [&](uint32_t bar, uint32_t parity) {
+            if (!broken && !mbar_wait(bar, parity, kWaitLimitNs)) {
+                broken = true;
+                if (lane == 0)
+                    atomicOr(&g_error, kErrCopyTimeout);
+            }
+        };
+
+        // the first row of every statistics warp now; the rest of the ring
+        // once those have landed, so the first rows arrive as early as they can
+        if (threadIdx.x == 0)
+            for (int64_t r = 0; r < kStatWarps && r < nrows; ++r)
+                issue(r);
+        for (int c = threadIdx.x; c < Dv; c += blockDim.x) {
+            c_s1[c] = bf2x4_add(ld_cached(scale + b * a.mod_bstride + c), kBf2One);
+            c_sh[c] = ld_cached(shift + b * a.mod_bstride + c);
+            if (kWeighted && has_w)
+                c_w[c] = ld_cached(weight + c);
+        }
+        __syncthreads();
+
+        if (warp < kStatWarps) {
+            // ---- statistics warps
+            for (int64_t r = warp; r < nrows; r += kStatWarps) {
+                const int s = slot_of(r);
+                wait(smem_addr(&full_bar[s]), parity_of(r));
+                if (r + kStatWarps < kSlots && lane == 0)
+                    issue(r + kStatWarps);  // the ring's second half, once
+                const uint4* buf = ring + s * kSegVec;
+                uint32_t m = 0;
+#pragma unroll
+                for (int j = 0; j < V; ++j) {
+                    const int v = j * 32 + lane;
+                    if (EXACT || v < Dv) {
+                        const uint4 xv = buf[v];
+                        m = bf2_absmax(m, bf2_absmax(bf2_absmax(xv.x, xv.y),
+                                                     bf2_absmax(xv.z, xv.w)));
+                    }
+                }
+                const uint32_t mm = absmax_bits(m);
+                const uint32_t E = offset_exponent(mm);
+                ExactSums<kNeedSum> acc;
+                acc.init(offset_k1<kL>(E), offset_k2<kL>(E));
+#pragma unroll 4
+                for (int j = 0; j < V; ++j) {
+                    const int v = j * 32 + lane;
+                    if (EXACT || v < Dv) {
+                        const uint4 xv = buf[v];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            acc.add(f2_from_bf2(word(xv, i)));
+                    }
+                }
+                float s1h, s1l, s2h, s2l;
+                acc.lane_total(s1h, s1l, s2h, s2l);
+                if (kNeedSum)
+                    dd2_allreduce<32>(s1h, s1l, s2h, s2l);
+                else
+                    dd_allreduce<32>(s2h, s2l);
+                const uint32_t cls =
+                    __reduce_max_sync(kFullMask, static_cast<uint32_t>(magnitude_class(mm)));
+                const uint32_t emax = __reduce_max_sync(kFullMask, mm == 0 ? 0u : (mm >> 7));
+                float mean = 0.0f, stat;
+                if (cls == kClassFast) {
+                    if (kNeedSum)
+                        finalize_ln(s1h, s1l, s2h, s2l, a.n, a.inv_n, mean, stat);
+                    else
+                        stat = finalize_ms(s2h, s2l, a.n, a.inv_n);
+                } else {
+                    slow_stats_smem<kNeedSum, V, kL, EXACT>(buf, Dv, cls, emax, lane, a.n,
+                                                            a.inv_n, mean, stat);
+                }
+                const float rstd = rstd_from(stat, a.eps);
+                if (lane == 0) {
+                    const int64_t row = r_begin + r;
+                    if (a.mean_out)
+                        a.mean_out[row] = mean;
+                    if (a.rstd_out)
+                        a.rstd_out[row] = rstd;
+                    slot_stats[s] = make_float2(mean, rstd);
+                    mbar_arrive(smem_addr(&ready_bar[s]));
+                }
+                __syncwarp();
+            }
+        } else {
+            // ---- output warps
+            const int ow = warp - kStatWarps;
+            for (int64_t r = ow; r < nrows; r += kOutWarps) {
+                const int s = slot_of(r);
+                wait(smem_addr(&ready_bar[s]), parity_of(r));
+                const float2 st = slot_stats[s];
+                const uint4* buf = ring + s * kSegVec;
+                const int64_t base = (r_begin + r) * Dv;
+                const u64 mean2 = f2_splat(st.x), rstd2 = f2_splat(st.y);
+#pragma unroll 4
+                for (int j = 0; j < V; ++j) {
+                    const int v = j * 32 + lane;
+                    if (EXACT || v < Dv) {
+                        const uint4 w =
+                            (kWeighted && has_w) ? c_w[v] : make_uint4(0u, 0u, 0u, 0u);
+                        st_stream(out + base + v, normalise_modulate<OP>(buf[v], mean2, rstd2,
+                                                                         c_s1[v], c_sh[v], w,
+                                                                         has_w));
+                    }
+                }
+                // the slot is consumed (its statistics warp finished reading
+                // before it arrived): refill it with the row kSlots ahead
+                __syncwarp();
+                if (lane == 0)
+                    issue(r + kSlots);
+            }
+        }
+        uses += nrows;
+        __syncthreads();  // the ring and the cache are free for the next item
+    }
+    if (broken)
+        drain_pause();
+}
+
+template <int OP, int V, bool EXACT>
+cudaError_t launch_ws(const RowArgs& a, const DeviceInfo& dev, cudaStream_t stream)
+{
+    using Shape = WsShape<OP, V>;
+    auto kern = row_kernel_ws<OP, V, EXACT>;
+    constexpr int kSmemMax = Shape::kRingBytes + Shape::kCacheBytes;
+    static int blocks_per_sm[64] = {0};
+    const int d = dev.device & 63;
+    if (blocks_per_sm[d] == 0) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+        if (e != cudaSuccess)
+            return e;
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Shape::kThreads, kSmemMax);
+        if (e != cudaSuccess)
+            return e;
+        blocks_per_sm[d] = n > 0 ? n : 1;
+    }
+    const int64_t cap = static_cast<int64_t>(dev.sms) * blocks_per_sm[d];
+    const int64_t B = a.rows / a.S;
+    int64_t per_batch = cap / (B > 0 ? B : 1);
+    const int64_t max_items = (a.S + Shape::kStatWarps - 1) / Shape::kStatWarps;
+    if (per_batch > max_items)
+        per_batch = max_items;
+    if (per_batch < 1)
+        per_batch = 1;
+    Items items;
+    items.per_batch = per_batch;
+    items.chunk = (a.S + per_batch - 1) / per_batch;
+    items.count = B * per_batch;
+    const int grid = static_cast<int>(items.count < cap ? items.count : cap);
+    const int smem = Shape::kRingBytes + Shape::kNmod * a.Dv * 16;
+    return launch_dependent(kern, grid, Shape::kThreads, smem, stream, a, items);
+}
+
 template <int OP, int V, int WPR, bool EXACT>
 cudaError_t launch_shape(const RowArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
@@ -500,6 +807,11 @@ cudaError_t launch_shape(const RowArgs& a, const DeviceInfo& dev, cudaStream_t s
 template <int OP, int V, int WPR>
 cudaError_t launch_cfg(const RowArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
+    if constexpr (OP != kOpGated && WPR == 1 && V == 12) {
+        if (a.Dv == 32 * V)
+            return launch_ws<OP, V, true>(a, dev, stream);
+        return launch_ws<OP, V, false>(a, dev, stream);
+    }
     if (a.Dv == 32 * V * WPR)
         return launch_shape<OP, V, WPR, true>(a, dev, stream);
     return launch_shape<OP, V, WPR, false>(a, dev, stream);

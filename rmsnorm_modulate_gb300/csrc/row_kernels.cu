@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads, RowShape<OP, V
 
 // ---------------------------------------------------------------------------
 // Warp-specialised variant for one warp per row (LN / RMS / folded LN,
-// 2048 < D <= 3072).  The CTA owns a ring of kSlots row buffers fed by 1-D
+// 2048 < D <= 4096).  The CTA owns a ring of kSlots row buffers fed by 1-D
 // bulk copies.  Statistics warps take rows in turn and stream them from
 // shared memory (abs-max, exact sums, butterfly, finalisation, rstd), leave
 // mean / rstd beside the row and arrive on the slot's "ready" barrier;
@@ -467,22 +467,29 @@ __global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads, RowShape<OP, V
 // of others instead of running in lock-step phases.
 // ---------------------------------------------------------------------------
 
+// Rows up to 3072 values: 8 statistics + 4 output warps, two CTAs per SM;
+// 4096 values: 8 + 8 warps and one CTA per SM with a 176 KB ring (the
+// epilogue's share of the work grows with the weight row of RMSNorm).
 template <int OP, int V>
 struct WsShape {
     static constexpr int kStatWarps = 8;
-    static constexpr int kOutWarps = 4;
+    static constexpr int kOutWarps = V >= 16 ? 8 : 4;
+    static constexpr int kBlocks = V >= 16 ? 1 : 2;
+    static constexpr int kRingBudget = (V >= 16 ? 176 : 100) * 1024;
     static constexpr int kWarps = kStatWarps + kOutWarps;
     static constexpr int kThreads = 32 * kWarps;
     static constexpr int kSegVec = 32 * V;
-    static constexpr int kNmod = (OP == kOpLN || OP == kOpLNFold) ? 2 : 3;
+    static constexpr int kNbuf = (OP == kOpGated) ? 2 : 1;  // residual + update
+    static constexpr int kSlotVec = kNbuf * kSegVec;
+    static constexpr int kNmod = (OP == kOpLN || OP == kOpLNFold) ? 2 : (OP == kOpRMS ? 3 : 4);
     static constexpr int kCacheBytes = kNmod * 32 * V * 16;
     // Rows r and r + kSlots share a slot; with kSlots a multiple of both warp
     // counts they also share their statistics warp and their output warp,
     // which take their rows in order, so no barrier is ever waited on with
     // the parity of a phase two steps ahead (which would read as complete).
-    static constexpr int kSlotsRaw = (100 * 1024) / (kSegVec * 16);
+    static constexpr int kSlotsRaw = kRingBudget / (kSlotVec * 16);
     static constexpr int kSlots = kSlotsRaw / kStatWarps * kStatWarps;
-    static constexpr int kRingBytes = kSlots * kSegVec * 16;
+    static constexpr int kRingBytes = kSlots * kSlotVec * 16;
     static_assert(kSlots >= kStatWarps && kSlots % kStatWarps == 0 && kSlots % kOutWarps == 0,
                   "a slot must return to the same statistics and output warps");
 };
@@ -540,19 +547,19 @@ __device__ __noinline__ void slow_stats_smem(const uint4* buf, int Dv, uint32_t 
 }
 
 template <int OP, int V, bool EXACT>
-__global__ void __launch_bounds__(WsShape<OP, V>::kThreads, 2)
+__global__ void __launch_bounds__(WsShape<OP, V>::kThreads, WsShape<OP, V>::kBlocks)
     row_kernel_ws(const RowArgs a, const Items items)
 {
     grid_dependency_sync();
     using Shape = WsShape<OP, V>;
     constexpr int kSlots = Shape::kSlots;
     constexpr int kSegVec = Shape::kSegVec;
+    constexpr int kSlotVec = Shape::kSlotVec;
     constexpr int kStatWarps = Shape::kStatWarps;
     constexpr int kOutWarps = Shape::kOutWarps;
     constexpr int kL = Log2Ceil<8 * V>::value;
     constexpr bool kNeedSum = (OP == kOpLN || OP == kOpLNFold);
-    constexpr bool kWeighted = (OP == kOpRMS);
-    static_assert(OP != kOpGated, "the gated op keeps the register-ring kernel");
+    constexpr bool kWeighted = (OP == kOpRMS || OP == kOpGated);
 
     extern __shared__ __align__(128) uint4 ring[];
     __shared__ __align__(8) unsigned long long full_bar[kSlots], ready_bar[kSlots];
@@ -563,7 +570,10 @@ __global__ void __launch_bounds__(WsShape<OP, V>::kThreads, 2)
     const int Dv = a.Dv;
     const uint32_t row_bytes = static_cast<uint32_t>(Dv) * 16u;
 
-    const uint4* __restrict__ src = static_cast<const uint4*>(a.x);
+    const uint4* __restrict__ src = static_cast<const uint4*>(OP == kOpGated ? a.residual : a.x);
+    const uint4* __restrict__ src1 = static_cast<const uint4*>(a.update);
+    const uint4* __restrict__ gate = static_cast<const uint4*>(a.gate);
+    uint4* __restrict__ res_out = static_cast<uint4*>(a.res_out);
     const uint4* __restrict__ weight = static_cast<const uint4*>(a.weight);
     const uint4* __restrict__ scale = static_cast<const uint4*>(a.scale);
     const uint4* __restrict__ shift = static_cast<const uint4*>(a.shift);
@@ -574,6 +584,7 @@ __global__ void __launch_bounds__(WsShape<OP, V>::kThreads, 2)
     uint4* c_s1 = cache;
     uint4* c_sh = cache + Dv;
     uint4* c_w = cache + 2 * Dv;
+    uint4* c_g = cache + 3 * Dv;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kSlots; ++s) {
@@ -604,8 +615,11 @@ __global__ void __launch_bounds__(WsShape<OP, V>::kThreads, 2)
             const int s = slot_of(r);
             const uint32_t bar = smem_addr(&full_bar[s]);
             fence_proxy_async();
-            mbar_expect_tx(bar, row_bytes);
-            bulk_g2s(smem_addr(ring + s * kSegVec), src + (r_begin + r) * Dv, row_bytes, bar);
+            mbar_expect_tx(bar, Shape::kNbuf * row_bytes);
+            bulk_g2s(smem_addr(ring + s * kSlotVec), src + (r_begin + r) * Dv, row_bytes, bar);
+            if (OP == kOpGated)
+                bulk_g2s(smem_addr(ring + s * kSlotVec + kSegVec), src1 + (r_begin + r) * Dv,
+                         row_bytes, bar);
         };
         auto wait = [&](uint32_t bar, uint32_t parity) {
             if (!broken && !mbar_wait(bar, parity, kWaitLimitNs)) {
@@ -625,6 +639,8 @@ __global__ void __launch_bounds__(WsShape<OP, V>::kThreads, 2)
             c_sh[c] = ld_cached(shift + b * a.mod_bstride + c);
             if (kWeighted && has_w)
                 c_w[c] = ld_cached(weight + c);
+            if (OP == kOpGated)
+                c_g[c] = ld_cached(gate + b * a.gate_bstride + c);
         }
         __syncthreads();
 
@@ -635,17 +651,31 @@ __global__ void __launch_bounds__(WsShape<OP, V>::kThreads, 2)
                 wait(smem_addr(&full_bar[s]), parity_of(r));
                 if (r + kStatWarps < kSlots && lane == 0)
                     issue(r + kStatWarps);  // the ring's second half, once
-                const uint4* buf = ring + s * kSegVec;
+                uint4* buf = ring + s * kSlotVec;
                 uint32_t m = 0;
 #pragma unroll
                 for (int j = 0; j < V; ++j) {
                     const int v = j * 32 + lane;
                     if (EXACT || v < Dv) {
-                        const uint4 xv = buf[v];
+                        uint4 xv = buf[v];
+                        if (OP == kOpGated) {
+                            // the residual stream res = R(residual + R(gate * update)):
+                            // written out, and over the residual in the slot for
+                            // the statistics and the output warp
+                            const uint4 u = buf[kSegVec + v], g = c_g[v];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                word(xv, i) = bf2_add(word(xv, i), bf2_mul(word(g, i), word(u, i)));
+                            buf[v] = xv;
+                            st_stream(res_out + (r_begin + r) * Dv + v, xv);
+                        }
                         m = bf2_absmax(m, bf2_absmax(bf2_absmax(xv.x, xv.y),
                                                      bf2_absmax(xv.z, xv.w)));
                     }
                 }
+                if (OP == kOpGated)
+                    fence_proxy_async();  // res written over the slot, which the
+                                          // async proxy refills later
                 const uint32_t mm = absmax_bits(m);
                 const uint32_t E = offset_exponent(mm);
                 ExactSums<kNeedSum> acc;
@@ -698,7 +728,7 @@ __global__ void __launch_bounds__(WsShape<OP, V>::kThreads, 2)
                 const int s = slot_of(r);
                 wait(smem_addr(&ready_bar[s]), parity_of(r));
                 const float2 st = slot_stats[s];
-                const uint4* buf = ring + s * kSegVec;
+                const uint4* buf = ring + s * kSlotVec;
                 const int64_t base = (r_begin + r) * Dv;
                 const u64 mean2 = f2_splat(st.x), rstd2 = f2_splat(st.y);
 #pragma unroll 4
@@ -807,7 +837,7 @@ cudaError_t launch_shape(const RowArgs& a, const DeviceInfo& dev, cudaStream_t s
 template <int OP, int V, int WPR>
 cudaError_t launch_cfg(const RowArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
-    if constexpr (OP != kOpGated && WPR == 1 && V == 12) {
+    if constexpr (WPR == 1 && (V == 16 || (V == 12 && OP != kOpGated))) {
         if (a.Dv == 32 * V)
             return launch_ws<OP, V, true>(a, dev, stream);
         return launch_ws<OP, V, false>(a, dev, stream);

@@ -491,7 +491,8 @@ cudaError_t launch_backward(BwdArgs a, const DeviceInfo& dev, cudaStream_t strea
     if (a.grad_scale || a.grad_shift) {
         const int64_t l1 = a.B * a.nblk * a.Dv * 2 * 4;  // four lanes per group
         int64_t g1 = (l1 + kTokThreads - 1) / kTokThreads;
-        const int64_t cap = static_cast<int64_t>(dev.sms) * 12;
+        // a persistent grid (four CTAs per SM loop over the blocks)
+        const int64_t cap = static_cast<int64_t>(dev.sms) * 4;
         e = launch_dependent(tokens_l1_kernel, static_cast<int>(g1 < cap ? g1 : cap),
                              kTokThreads, 0, stream, a);
         if (e != cudaSuccess)

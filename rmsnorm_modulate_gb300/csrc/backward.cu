@@ -54,6 +54,63 @@ __device__ __forceinline__ void dd_acc(u64& hi, u64& lo, u64 v)
     hi = s;
 }
 
+// Pass 1 of one row (one warp; x, g and s1 rows in shared memory):
+//   c1 = fp32(sum dyhat / D), c2 = fp32(sum dyhat * yhat / D)
+// with both sums carried as double-float values (TwoSum per value, TwoProd
+// for dyhat * yhat), so each is the exact sum up to the rounding of its low
+// word; all lanes return both.
+// S1_GLOBAL: s1 is formed here from the scale row in global memory (s1buf
+// points there) instead of read ready-made from shared memory.
+template <bool S1_GLOBAL>
+__device__ __forceinline__ void row_c1c2(const uint4* xbuf, const uint4* gbuf, const uint4* s1buf,
+                                         int Dv, int lane, u64 mean2, u64 rstd2, float n,
+                                         float inv_n, float& c1, float& c2)
+{
+    u64 h1 = 0, l1 = 0, h2 = 0, l2 = 0, e2 = 0;
+#pragma unroll 2
+    for (int v = lane; v < Dv; v += 32) {
+        const uint4 xv = xbuf[v], gv = gbuf[v];
+        const uint4 sv = S1_GLOBAL ? bf2x4_add(ld_cached(s1buf + v), kBf2One) : s1buf[v];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const u64 yhat = f2_mul(f2_sub(f2_from_bf2(word(xv, i)), mean2), rstd2);
+            const u64 dy = f2_mul(f2_from_bf2(word(gv, i)), f2_from_bf2(word(sv, i)));
+            dd_acc(h1, l1, dy);
+            // p = RN(dyhat * yhat) as separately rounded products (a packed
+            // product feeding the TwoSum could be contracted into it); e =
+            // the exact product error (TwoProd)
+            float d0, d1, y0, y1;
+            f2_unpack(dy, d0, d1);
+            f2_unpack(yhat, y0, y1);
+            const u64 p = f2_pack(__fmul_rn(d0, y0), __fmul_rn(d1, y1));
+            e2 = f2_add(e2, f2_fma(dy, yhat, f2_neg(p)));
+            dd_acc(h2, l2, p);
+        }
+    }
+    l2 = f2_add(l2, e2);
+    // the two lanes of each pair, then the warp
+    float s1h, s1l, s2h, s2l;
+    {
+        float a0, a1, b0, b1;
+        f2_unpack(h1, a0, a1);
+        f2_unpack(l1, b0, b1);
+        s1h = a0;
+        s1l = b0;
+        dd_add(s1h, s1l, a1, b1);
+        f2_unpack(h2, a0, a1);
+        f2_unpack(l2, b0, b1);
+        s2h = a0;
+        s2l = b0;
+        dd_add(s2h, s2l, a1, b1);
+    }
+    dd2_allreduce<32>(s1h, s1l, s2h, s2l);
+    float q1, q2;
+    dd_div_n(s1h, s1l, n, inv_n, q1, q2);
+    c1 = __fadd_rn(q1, q2);
+    dd_div_n(s2h, s2l, n, inv_n, q1, q2);
+    c2 = __fadd_rn(q1, q2);
+}
+
 __global__ void __launch_bounds__(kDxThreads, 2) dx_kernel(const BwdArgs a)
 {
     grid_dependency_sync();
@@ -117,48 +174,8 @@ __global__ void __launch_bounds__(kDxThreads, 2) dx_kernel(const BwdArgs a)
             const u64 mean2 = f2_splat(mean), rstd2 = f2_splat(rstd);
 
             // ---- pass 1: c1 = sum dyhat, c2 = sum dyhat * yhat (double-float)
-            u64 h1 = 0, l1 = 0, h2 = 0, l2 = 0, e2 = 0;
-#pragma unroll 2
-            for (int v = lane; v < Dv; v += 32) {
-                const uint4 xv = xbuf[v], gv = gbuf[v], sv = c_s1[v];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const u64 yhat = f2_mul(f2_sub(f2_from_bf2(word(xv, i)), mean2), rstd2);
-                    const u64 dy = f2_mul(f2_from_bf2(word(gv, i)), f2_from_bf2(word(sv, i)));
-                    dd_acc(h1, l1, dy);
-                    // p = RN(dyhat * yhat) as separately rounded products (a
-                    // packed product feeding the TwoSum could be contracted
-                    // into it); e = the exact product error (TwoProd)
-                    float d0, d1, y0, y1;
-                    f2_unpack(dy, d0, d1);
-                    f2_unpack(yhat, y0, y1);
-                    const u64 p = f2_pack(__fmul_rn(d0, y0), __fmul_rn(d1, y1));
-                    e2 = f2_add(e2, f2_fma(dy, yhat, f2_neg(p)));
-                    dd_acc(h2, l2, p);
-                }
-            }
-            l2 = f2_add(l2, e2);
-            // the two lanes of each pair, then the warp
-            float s1h, s1l, s2h, s2l;
-            {
-                float a0, a1, b0, b1;
-                f2_unpack(h1, a0, a1);
-                f2_unpack(l1, b0, b1);
-                s1h = a0;
-                s1l = b0;
-                dd_add(s1h, s1l, a1, b1);
-                f2_unpack(h2, a0, a1);
-                f2_unpack(l2, b0, b1);
-                s2h = a0;
-                s2l = b0;
-                dd_add(s2h, s2l, a1, b1);
-            }
-            dd2_allreduce<32>(s1h, s1l, s2h, s2l);
-            float q1, q2;
-            dd_div_n(s1h, s1l, n, inv_n, q1, q2);
-            const float c1 = __fadd_rn(q1, q2);
-            dd_div_n(s2h, s2l, n, inv_n, q1, q2);
-            const float c2 = __fadd_rn(q1, q2);
+            float c1, c2;
+            row_c1c2<false>(xbuf, gbuf, c_s1, Dv, lane, mean2, rstd2, n, inv_n, c1, c2);
 
             // ---- pass 2: grad_x = R(rstd * ((dyhat - c1) - yhat * c2))
             const int64_t base = row * Dv;
@@ -416,6 +433,434 @@ __global__ void __launch_bounds__(kTokThreads) tokens_up_kernel(const BwdArgs a)
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// grad_x and the first token-tree level in one pass over HBM
+// ---------------------------------------------------------------------------
+//
+// Warp-specialised, one CTA per SM walking its blocks (batch b, block j of
+// 32 tokens) in order; the rows of those blocks form the CTA's sequence, and
+// row i of the sequence lands by bulk copy (x row, then g row) in slot
+// i % nslots of a shared-memory ring.
+//   output warps (Wout = Dv / 32; thread t owns the 8 columns of vector t)
+//       take every row in sequence order: grad_x of their columns, and both
+//       token trees of the block for them (binary counter over the 32 slots,
+//       +0 past the end; levels 0-1 in registers, 2-4 in shared memory)
+//   statistics warps (kBwdStatWarps) take rows i = w, w + 8, ...: c1, c2
+//       into the slot's statistics, then the slot's ready barrier
+// Each output warp releases a slot with one atomic add; the last of them
+// refills it with the row nslots further on, after tagging the slot with that
+// row's sequence number.  A statistics warp may reach a slot before the
+// previous fill of it has landed (its rows are not those nslots apart), where
+// the barrier's parity would alias; it checks the tag first.  x and g are
+// read from HBM once.
+
+constexpr int kBwdStatWarps = 8;
+constexpr int kBwdMaxOutWarps = 12;  // D <= 3072
+constexpr int kBwdMinOutWarps = 4;   // D >= 1024
+constexpr int kBwdMaxSlots = 32;
+
+__device__ __forceinline__ void st_release_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Release of a slot by one output warp (lane 0, after __syncwarp): returns
+// the count before this add (acquire-release, so the last releaser sees every
+// warp's reads of the slot as done).
+__device__ __forceinline__ uint32_t release_add(uint32_t addr)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                 : "=r"(old)
+                 : "r"(addr)
+                 : "memory");
+    return old;
+}
+
+// One block of the sequence: batch b, block j of 32 tokens (item = b * nblk
+// + j; item counts fit in 32 bits).
+struct SeqBlock {
+    int64_t r0;  // its first row
+    int64_t b;
+    int nrows;   // 0: past the end of the sequence
+};
+
+struct BwdSeq {
+    uint32_t items, stride, nblk;
+    int64_t S;
+
+    __device__ __forceinline__ SeqBlock block(uint32_t item) const
+    {
+        if (item >= items)
+            return SeqBlock{0, 0, 0};
+        const uint32_t b = item / nblk, j = item - b * nblk;
+        const int64_t left = S - 32 * static_cast<int64_t>(j);
+        return SeqBlock{static_cast<int64_t>(b) * S + 32 * static_cast<int64_t>(j),
+                        static_cast<int64_t>(b), static_cast<int>(left < 32 ? left : 32)};
+    }
+};
+
+// A walk along the sequence (one division per block entered).
+struct SeqCursor {
+    uint32_t item;
+    int r;
+    SeqBlock blk;
+
+    __device__ __forceinline__ void start(const BwdSeq& sq, uint32_t first)
+    {
+        item = first;
+        r = 0;
+        blk = sq.block(first);
+    }
+
+    __device__ __forceinline__ bool done() const { return blk.nrows == 0; }
+
+    __device__ __forceinline__ int64_t row() const { return blk.r0 + r; }
+
+    __device__ __forceinline__ void advance(const BwdSeq& sq, int by)
+    {
+        r += by;
+        while (blk.nrows != 0 && r >= blk.nrows) {
+            r -= blk.nrows;
+            item += sq.stride;
+            blk = sq.block(item);
+        }
+    }
+};
+
+// Ring slot and fill parity of a sequence position, advanced in step with it.
+struct SlotPos {
+    uint32_t slot, par, round;
+
+    __device__ __forceinline__ void advance(uint32_t by, uint32_t ns)
+    {
+        slot += by;
+        while (slot >= ns) {
+            slot -= ns;
+            par ^= 1u;
+            ++round;
+        }
+    }
+};
+
+// The two token trees of one 32-token block for 8 columns (4 packed pairs):
+// a binary counter over the slots, the slot index known at run time.  Level
+// l holds a finished subtree of 2^l slots while bit l of the count is set;
+// the left operand of every add is the earlier subtree.  Levels 0-1 are
+// registers, levels 2-4 this thread's columns of up[3][8][nthreads] in
+// shared memory (written at most every 4th slot).
+struct BlockTrees {
+    u64 g[2][4], p[2][4];
+    u64* up;     // &up[0][0][t]
+    int stride;  // nthreads
+
+    __device__ __forceinline__ u64& lvl(int l, int q, int i) const
+    {
+        return up[((l - 2) * 8 + q * 4 + i) * stride];
+    }
+
+    // Pushes slot k's values of pair i, with ones = the number of trailing
+    // one bits of k: the finished subtrees below the first clear bit join the
+    // new value (lowest level first), which then takes that bit's level; slot
+    // 31 closes the tree at level 4.  Predicated, so the register levels stay
+    // in registers.
+    __device__ __forceinline__ void push(int ones, int i, u64 vg, u64 vp)
+    {
+#pragma unroll
+        for (int l = 0; l < 2; ++l) {
+            if (l < ones) {
+                vg = f2_add(g[l][i], vg);
+                vp = f2_add(p[l][i], vp);
+            }
+        }
+        if (ones < 2) {
+#pragma unroll
+            for (int l = 0; l < 2; ++l) {
+                if (l == ones) {
+                    g[l][i] = vg;
+                    p[l][i] = vp;
+                }
+            }
+            return;
+        }
+        for (int l = 2; l < ones && l < 5; ++l) {
+            vg = f2_add(lvl(l, 0, i), vg);
+            vp = f2_add(lvl(l, 1, i), vp);
+        }
+        const int dst = ones < 4 ? ones : 4;
+        lvl(dst, 0, i) = vg;
+        lvl(dst, 1, i) = vp;
+    }
+};
+
+__global__ void __launch_bounds__(32 * (kBwdMaxOutWarps + kBwdStatWarps), 1)
+    bwd_ws_kernel(const BwdArgs a, const int nslots)
+{
+    grid_dependency_sync();
+    extern __shared__ __align__(128) uint4 smem[];
+    __shared__ __align__(8) unsigned long long full_bar[kBwdMaxSlots], ready_bar[kBwdMaxSlots];
+    __shared__ float4 slot_stats[kBwdMaxSlots];  // (mean, rstd, c1, c2) of the row in each slot
+    __shared__ uint32_t released[kBwdMaxSlots];  // output-warp releases, cumulative
+    __shared__ uint32_t slot_seq[kBwdMaxSlots];  // sequence number of the slot's latest fill
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int Dv = a.Dv;
+    const int Wout = Dv >> 5;
+    const int nout = 32 * Wout;
+    const uint32_t ns = static_cast<uint32_t>(nslots);
+    const uint32_t row_bytes = static_cast<uint32_t>(Dv) * 16u;
+    uint4* ring = smem;                                                   // [nslots][x, g][Dv]
+    u64* up = reinterpret_cast<u64*>(ring + static_cast<size_t>(nslots) * 2 * Dv);  // [3][8][nout]
+
+    const uint4* __restrict__ xg = static_cast<const uint4*>(a.x);
+    const uint4* __restrict__ gg = static_cast<const uint4*>(a.grad_out);
+    const BwdSeq sq{static_cast<uint32_t>(a.B * a.nblk), gridDim.x,
+                    static_cast<uint32_t>(a.nblk), a.S};
+
+    // the copy of `row` (sequence number q) into slot s (one thread)
+    auto issue = [&](int64_t row, uint32_t s, uint32_t q) {
+        const uint32_t bar = smem_addr(&full_bar[s]);
+        uint4* dst = ring + static_cast<size_t>(s) * 2 * Dv;
+        st_release_u32(smem_addr(&slot_seq[s]), q);
+        fence_proxy_async();
+        mbar_expect_tx(bar, 2u * row_bytes);
+        bulk_g2s(smem_addr(dst), xg + row * Dv, row_bytes, bar);
+        bulk_g2s(smem_addr(dst + Dv), gg + row * Dv, row_bytes, bar);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nslots; ++s) {
+            mbar_init(smem_addr(&full_bar[s]), 1u);
+            mbar_init(smem_addr(&ready_bar[s]), 1u);
+            released[s] = 0;
+        }
+        mbar_init_fence();
+        // the first nslots rows of the sequence
+        SeqCursor c;
+        c.start(sq, blockIdx.x);
+        for (uint32_t s = 0; s < ns && !c.done(); ++s) {
+            issue(c.row(), s, s);
+            c.advance(sq, 1);
+        }
+    }
+    __syncthreads();
+
+    bool broken = false;
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (!broken && !mbar_wait_sleep(bar, parity, kWaitLimitNs)) {
+            broken = true;
+            atomicOr(&g_error, kErrCopyTimeout);
+        }
+    };
+
+    if (warp >= Wout) {
+        // ---- statistics warps: rows w, w + 8, ... of the sequence
+        const int sw = warp - Wout;
+        const uint4* __restrict__ scale = static_cast<const uint4*>(a.scale);
+        const float n = a.n, inv_n = a.inv_n;
+        SeqCursor c;
+        c.start(sq, blockIdx.x);
+        c.advance(sq, sw);
+        SlotPos sp{0, 0, 0};
+        sp.advance(static_cast<uint32_t>(sw), ns);
+        uint32_t q = static_cast<uint32_t>(sw);  // sequence number of the row
+        while (!c.done()) {
+            const uint32_t s = sp.slot;
+            const int64_t row = c.row();
+            const int64_t b = c.blk.b;
+            // the row's forward statistics load while its copy lands
+            const float mean = a.mean[row], rstd = a.rstd[row];
+            // the slot's fill for this row is issued (so the fill before it
+            // has landed), then the fill itself
+            const uint32_t tag = smem_addr(&slot_seq[s]);
+            if (!broken && ld_acquire_u32(tag) != q) {
+                const unsigned long long t0 = global_ns();
+                while (ld_acquire_u32(tag) != q) {
+                    __nanosleep(64);
+                    if (global_ns() - t0 > kWaitLimitNs) {
+                        broken = true;
+                        atomicOr(&g_error, kErrCopyTimeout);
+                        break;
+                    }
+                }
+            }
+            wait(smem_addr(&full_bar[s]), sp.par);
+            const uint4* xbuf = ring + static_cast<size_t>(s) * 2 * Dv;
+            float c1, c2;
+            row_c1c2<true>(xbuf, xbuf + Dv, scale + b * a.mod_bstride, Dv, lane, f2_splat(mean),
+                           f2_splat(rstd), n, inv_n, c1, c2);
+            if (lane == 0) {
+                slot_stats[s] = make_float4(mean, rstd, c1, c2);
+                mbar_arrive(smem_addr(&ready_bar[s]));
+            }
+            __syncwarp();
+            c.advance(sq, kBwdStatWarps);
+            sp.advance(kBwdStatWarps, ns);
+            q += kBwdStatWarps;
+        }
+        if (broken)
+            drain_pause();
+        return;
+    }
+
+    // ---- output warps
+    const int t = threadIdx.x;  // this thread's vector of 8 columns
+    const uint4* __restrict__ scale = static_cast<const uint4*>(a.scale);
+    uint4* __restrict__ gx = static_cast<uint4*>(a.grad_x);
+    float4* __restrict__ ws = static_cast<float4*>(a.workspace);
+    SlotPos sp{0, 0, 0};
+    uint32_t seq = 0;  // sequence number of the next row
+    for (uint32_t item = blockIdx.x; item < sq.items; item += gridDim.x) {
+        const SeqBlock blk = sq.block(item);
+        const SeqBlock next = sq.block(item + gridDim.x);
+        const int64_t b = blk.b, r0 = blk.r0;
+        const int nrows = blk.nrows;
+        const uint4 s1v = bf2x4_add(ld_cached(scale + b * a.mod_bstride + t), kBf2One);
+        BlockTrees tr;
+        tr.up = up + t;
+        tr.stride = nout;
+#pragma unroll 1
+        for (int k = 0; k < 32; ++k) {
+            const int ones = __ffs(~k) - 1;  // trailing one bits of k
+            if (k < nrows) {
+                const uint32_t s = sp.slot;
+                wait(smem_addr(&ready_bar[s]), sp.par);
+                const uint4* xbuf = ring + static_cast<size_t>(s) * 2 * Dv;
+                const uint4 xv = xbuf[t], gv = xbuf[Dv + t];
+                const float4 st = slot_stats[s];
+                __syncwarp();
+                if (lane == 0) {
+                    // the slot is consumed by this warp; the last of the
+                    // output warps refills it with the row nslots further on
+                    const uint32_t old = release_add(smem_addr(&released[s]));
+                    if (old + 1u == static_cast<uint32_t>(Wout) * (sp.round + 1u)) {
+                        const int q = k + nslots;
+                        const uint32_t qseq = seq + ns;
+                        if (q < nrows) {
+                            issue(r0 + q, s, qseq);
+                        } else if (q - nrows < next.nrows) {
+                            issue(next.r0 + (q - nrows), s, qseq);
+                        } else {  // short blocks: walk on
+                            SeqCursor c;
+                            c.start(sq, item);
+                            c.advance(sq, q);
+                            if (!c.done())
+                                issue(c.row(), s, qseq);
+                        }
+                    }
+                }
+                sp.advance(1u, ns);
+                ++seq;
+                const u64 mean2 = f2_splat(st.x), rstd2 = f2_splat(st.y);
+                uint4 o;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const u64 yhat = f2_mul(f2_sub(f2_from_bf2(word(xv, i)), mean2), rstd2);
+                    const u64 gf = f2_from_bf2(word(gv, i));
+                    const u64 dy = f2_mul(gf, f2_from_bf2(word(s1v, i)));
+                    float y0, y1, d0, d1;
+                    f2_unpack(yhat, y0, y1);
+                    f2_unpack(dy, d0, d1);
+                    // grad_x = R(rstd * ((dyhat - c1) - R32(yhat * c2)))
+                    const float t0 = __fsub_rn(__fsub_rn(d0, st.z), __fmul_rn(y0, st.w));
+                    const float t1 = __fsub_rn(__fsub_rn(d1, st.z), __fmul_rn(y1, st.w));
+                    word(o, i) = pack_bf2(__fmul_rn(st.y, t0), __fmul_rn(st.y, t1));
+                    // token-tree values: g, and g * R(yhat) (exact: two bf16)
+                    tr.push(ones, i, gf, f2_mul(gf, f2_from_bf2(bf2_from_f2(yhat))));
+                }
+                st_stream(gx + (r0 + k) * Dv + t, o);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    tr.push(ones, i, 0ull, 0ull);  // +0 past the end of the sequence
+            }
+        }
+
+        // the block's values -> workspace [B][nblk][2][D]: quantity 0 =
+        // grad_shift, 1 = grad_scale
+        float rg[8], rp[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f2_unpack(tr.lvl(4, 0, i), rg[2 * i], rg[2 * i + 1]);
+            f2_unpack(tr.lvl(4, 1, i), rp[2 * i], rp[2 * i + 1]);
+        }
+        const int64_t o = (static_cast<int64_t>(item) * 2) * (2 * Dv) + 2 * t;  // item = b nblk + j
+        ws[o] = make_float4(rg[0], rg[1], rg[2], rg[3]);
+        ws[o + 1] = make_float4(rg[4], rg[5], rg[6], rg[7]);
+        ws[o + 2 * Dv] = make_float4(rp[0], rp[1], rp[2], rp[3]);
+        ws[o + 2 * Dv + 1] = make_float4(rp[4], rp[5], rp[6], rp[7]);
+    }
+    if (broken)
+        drain_pause();
+}
+
+// Above the first level when 2 <= nblk <= 1024 (one level-2 node per run of
+// 32 block values, at most 32 of them): lane groups of P lanes (P = n2
+// rounded up to a power of two) per column and quantity, lane m forming
+// level-2 node m (its 32 loads issued together, +0 past nblk; lanes m >= n2
+// hold +0); a butterfly over the group gives the tree over P slots, and
+// adding +0 once per doubling up to 32 completes it to the 32-slot tree.  With
+// n2 == 1 the level-2 node is the result.  Lanes of a warp: m = lane / C, C =
+// 32 / P columns side by side, so every load instruction reads C adjacent
+// columns of P block rows.
+__global__ void __launch_bounds__(kTokThreads) tokens_top_kernel(const BwdArgs a, const int P)
+{
+    grid_dependency_sync();
+    const int D = a.Dv * 8;
+    const int C = 32 / P;
+    const int lane = threadIdx.x & 31;
+    const int m = lane / C, c = lane - m * C;
+    const int64_t nblk = a.nblk;
+    const int n2 = static_cast<int>((nblk + 31) / 32);
+    const int64_t warps_per_q = (D + C - 1) / C;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (warp >= a.B * 2 * warps_per_q)
+        return;  // whole warps only
+    const int64_t bq = warp / warps_per_q;
+    const int64_t b = bq >> 1;
+    const int q = static_cast<int>(bq & 1);  // 0: grad_shift, 1: grad_scale
+    const int d = static_cast<int>((warp - bq * warps_per_q) * C + c);
+    const bool active = d < D;
+    const float* col = static_cast<const float*>(a.workspace) +
+                       ((b * nblk) * 2 + q) * static_cast<int64_t>(D) + (active ? d : 0);
+    const int64_t stride = 2 * static_cast<int64_t>(D);
+
+    float v = 0.0f;
+    if (active && m < n2) {
+        float x[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const int64_t idx = 32 * static_cast<int64_t>(m) + k;
+            x[k] = idx < nblk ? col[idx * stride] : 0.0f;
+        }
+        ScalarTree<5> t;
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+            t.push(k, x[k]);
+        v = t.stack[4];
+    }
+    if (n2 > 1) {
+        for (int off = C; off < 32; off <<= 1)
+            v = __fadd_rn(v, __shfl_xor_sync(kFullMask, v, off));
+        for (int w = P; w < 32; w <<= 1)
+            v = __fadd_rn(v, 0.0f);  // the all-zero right subtree
+    }
+    if (active && m == 0) {
+        float* out = q == 0 ? a.grad_shift : a.grad_scale;
+        if (out)
+            out[b * D + d] = v;
+    }
+}
+
 }  // namespace
 
 // Fixed device scratch for ln_modulate_backward_static: the token-sum
@@ -450,9 +895,73 @@ size_t backward_workspace_bytes(int64_t B, int64_t S, int64_t D)
            sizeof(float);
 }
 
+// The token trees above the first level (block values in the workspace):
+// lane groups per column where at most 32 level-2 nodes exist, else one
+// thread per column.
+static cudaError_t launch_upper(const BwdArgs& a, const DeviceInfo& dev, cudaStream_t stream)
+{
+    if (a.nblk >= 2 && a.nblk <= 32 * 32) {
+        const int n2 = static_cast<int>((a.nblk + 31) / 32);
+        int P = 1;
+        while (P < n2)
+            P <<= 1;
+        const int64_t D = a.Dv * 8;
+        const int64_t lanes = a.B * 2 * ((D + 32 / P - 1) / (32 / P)) * 32;
+        const int64_t grid = (lanes + kTokThreads - 1) / kTokThreads;
+        return launch_dependent(tokens_top_kernel, static_cast<int>(grid), kTokThreads, 0,
+                                stream, a, P);
+    }
+    const int64_t up = a.B * a.Dv * 8;
+    const int64_t g2 = (up + kTokThreads - 1) / kTokThreads;
+    const int64_t cap = static_cast<int64_t>(dev.sms) * 4;
+    return launch_dependent(tokens_up_kernel, static_cast<int>(g2 < cap ? g2 : cap), kTokThreads,
+                            0, stream, a);
+}
+
+// grad_x and the token sums of one call through bwd_ws_kernel, then the
+// upper tree levels; false (nothing launched) where its shape rules do not
+// hold: S >= 2 (a one-token sequence takes no tree), D a multiple of 256
+// from 1024 to 3072.
+static bool launch_fused(const BwdArgs& a, const DeviceInfo& dev, cudaStream_t stream,
+                         cudaError_t& e)
+{
+    if (!a.grad_x || !(a.grad_scale || a.grad_shift) || a.S < 2 || a.Dv % 32 != 0)
+        return false;
+    const int Wout = a.Dv / 32;
+    if (Wout < kBwdMinOutWarps || Wout > kBwdMaxOutWarps)
+        return false;
+    // ring slots: as many as ~220 KB hold beside the upper tree levels
+    constexpr int kBudget = 220 * 1024;
+    const int slot_bytes = 2 * a.Dv * 16;
+    const int up_bytes = 3 * 8 * 32 * Wout * 8;
+    int nslots = (kBudget - up_bytes) / slot_bytes;
+    nslots = nslots > kBwdMaxSlots ? kBwdMaxSlots : nslots;
+    const int smem = nslots * slot_bytes + up_bytes;
+    const int threads = 32 * (Wout + kBwdStatWarps);
+    static bool configured[64] = {false};
+    const int d = dev.device & 63;
+    if (!configured[d]) {
+        e = cudaFuncSetAttribute(bwd_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kBudget);
+        if (e != cudaSuccess)
+            return true;
+        configured[d] = true;
+    }
+    const int64_t items = a.B * a.nblk;
+    const int64_t cap = dev.sms;  // one CTA per SM
+    e = launch_dependent(bwd_ws_kernel, static_cast<int>(items < cap ? items : cap), threads,
+                         smem, stream, a, nslots);
+    if (e != cudaSuccess)
+        return true;
+    e = launch_upper(a, dev, stream);
+    return true;
+}
+
 cudaError_t launch_backward(BwdArgs a, const DeviceInfo& dev, cudaStream_t stream)
 {
     cudaError_t e = cudaSuccess;
+    if (launch_fused(a, dev, stream, e))
+        return e;
     if (a.grad_x) {
         // warps per CTA: as many as ~200 KB of shared memory hold (x and g
         // rows per warp plus the s1 row), at most eight
@@ -497,10 +1006,7 @@ cudaError_t launch_backward(BwdArgs a, const DeviceInfo& dev, cudaStream_t strea
                              kTokThreads, 0, stream, a);
         if (e != cudaSuccess)
             return e;
-        const int64_t up = a.B * a.Dv * 8;
-        const int64_t g2 = (up + kTokThreads - 1) / kTokThreads;
-        e = launch_dependent(tokens_up_kernel, static_cast<int>(g2 < cap ? g2 : cap),
-                             kTokThreads, 0, stream, a);
+        e = launch_upper(a, dev, stream);
     }
     return e;
 }

@@ -60,6 +60,15 @@ def run(rm, oracle_mod, inp, want_exact_rows=0.99):
     (2, 1100, 256, True),   # 35 blocks: two tree levels above the first
     (1, 40, 3072, False),
     (1, 9, 16384, False),   # the largest D: one warp per CTA-share of shared memory
+    # the one-pass kernel (D a multiple of 256 from 1024 to 3072, S >= 2)
+    (3, 2, 1280, True),     # two-token sequences, five consumer warps
+    (2, 100, 2048, True),   # a 4-token last block, eight warps
+    (1, 40, 2560, False),   # ten warps
+    (2, 1100, 1024, True),  # 35 blocks per batch, two CTAs per SM
+    (3, 1700, 3072, True),  # more blocks than CTAs: each CTA loops over several
+    # the trees above the first level
+    (1, 32768, 8, False),   # 1024 blocks: 32 level-2 nodes, the widest lane groups
+    (1, 33000, 8, False),   # 1032 blocks: past the lane groups, one thread per column
 ])
 def test_shapes(rm, oracle_mod, B, S, D, per_batch):
     run(rm, oracle_mod, make(B, S, D, seed=B * 100 + S + D, per_batch=per_batch))
@@ -69,6 +78,48 @@ def test_flux_full_size(rm, oracle_mod):
     inp = make(1, 4608, 3072, seed=21)
     d = run(rm, oracle_mod, inp)
     assert (d == 0).mean() > 0.9999
+
+
+@pytest.mark.parametrize("need_x", [True, False])
+def test_one_pass_and_token_only_paths_agree(rm, need_x):
+    # the one-pass kernel (grad_x wanted) and the token-sum-only kernels give
+    # the same bits; each equals the oracle's in test_shapes
+    inp = make(2, 300, 2048, seed=25)
+    x, sc, g = dev(inp["x"]), dev(inp["scale"]), dev(inp["g"])
+    mean = torch.empty(600, dtype=torch.float32, device="cuda")
+    rstd = torch.empty_like(mean)
+    rm.ln_modulate(x, sc, dev(inp["shift"]), mean_out=mean, rstd_out=rstd)
+    _, gsc0, gsh0 = rm.ln_modulate_backward(x, sc, g, mean, rstd, need_x=False)
+    gx, gsc, gsh = rm.ln_modulate_backward(x, sc, g, mean, rstd, need_x=need_x)
+    assert torch.equal(gsc, gsc0) and torch.equal(gsh, gsh0)
+    if need_x:
+        gx_only, _, _ = rm.ln_modulate_backward(x, sc, g, mean, rstd, need_mod=False)
+        assert torch.equal(gx, gx_only)
+
+
+@pytest.mark.parametrize("which", ["grad_scale", "grad_shift"])
+def test_one_token_sum_requested(rm, which):
+    # the C ABI with one modulation gradient left out: the other is unchanged
+    B, S, D = 2, 300, 2048
+    inp = make(B, S, D, seed=26)
+    x, sc, g = dev(inp["x"]), dev(inp["scale"]), dev(inp["g"])
+    mean = torch.empty(B * S, dtype=torch.float32, device="cuda")
+    rstd = torch.empty_like(mean)
+    rm.ln_modulate(x, sc, dev(inp["shift"]), mean_out=mean, rstd_out=rstd)
+    gx, gsc, gsh = rm.ln_modulate_backward(x, sc, g, mean, rstd)
+    want = gsc if which == "grad_scale" else gsh
+    got = torch.full_like(want, float("nan"))
+    gx1 = torch.empty_like(gx)
+    ws = torch.empty(rm.backward_workspace_bytes(B, S, D), dtype=torch.uint8, device="cuda")
+    P = __import__("ctypes").c_void_p
+    ptr = lambda t: P(t.data_ptr())
+    st = rm.library().ln_modulate_backward(
+        ptr(x), ptr(sc), D, ptr(g), ptr(mean), ptr(rstd), B, S, D, ptr(gx1),
+        ptr(got) if which == "grad_scale" else None, ptr(got) if which == "grad_shift" else None,
+        ptr(ws), ws.numel(), P(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.equal(got, want) and torch.equal(gx1, gx)
 
 
 def test_token_sums_are_batch_invariant(rm):

@@ -551,53 +551,49 @@ struct SlotPos {
     }
 };
 
-// The two token trees of one 32-token block for 8 columns (4 packed pairs):
-// a binary counter over the slots, the slot index known at run time.  Level
-// l holds a finished subtree of 2^l slots while bit l of the count is set;
-// the left operand of every add is the earlier subtree.  Levels 0-1 are
-// registers, levels 2-4 this thread's columns of up[3][8][nthreads] in
-// shared memory (written at most every 4th slot).
+// The two token trees of one 32-token block for 8 columns (4 packed pairs)
+// as a binary counter over the slots: level l holds a finished subtree of
+// 2^l slots while bit l of the count is set, the left operand of every add is
+// the earlier subtree.  Rows come in groups of four (slot k = 4 m + i, i known
+// at compile time), so levels 0 and 1 are resolved in registers without
+// tests; each finished 4-slot subtree enters a counter over m with levels
+// 2-4 in this thread's columns of up[3][8][nthreads] in shared memory.
 struct BlockTrees {
-    u64 g[2][4], p[2][4];
-    u64* up;     // &up[0][0][t]
-    int stride;  // nthreads
+    u64 g0[4], p0[4], g1[4], p1[4];  // levels 0 and 1
+    u64* up;                         // &up[0][0][t]
+    int stride;                      // nthreads
 
     __device__ __forceinline__ u64& lvl(int l, int q, int i) const
     {
         return up[((l - 2) * 8 + q * 4 + i) * stride];
     }
 
-    // Pushes slot k's values of pair i, with ones = the number of trailing
-    // one bits of k: the finished subtrees below the first clear bit join the
-    // new value (lowest level first), which then takes that bit's level; slot
-    // 31 closes the tree at level 4.  Predicated, so the register levels stay
-    // in registers.
-    __device__ __forceinline__ void push(int ones, int i, u64 vg, u64 vp)
+    // slot 4 m + I, pair i
+    template <int I>
+    __device__ __forceinline__ void push(int m, int i, u64 vg, u64 vp)
     {
-#pragma unroll
-        for (int l = 0; l < 2; ++l) {
-            if (l < ones) {
-                vg = f2_add(g[l][i], vg);
-                vp = f2_add(p[l][i], vp);
+        if (I == 0 || I == 2) {
+            g0[i] = vg;
+            p0[i] = vp;
+        } else if (I == 1) {
+            g1[i] = f2_add(g0[i], vg);
+            p1[i] = f2_add(p0[i], vp);
+        } else {
+            // the 4-slot subtree (s0 + s1) + (s2 + s3), then the counter over
+            // m: the finished subtrees below the first clear bit of m join it,
+            // and it takes that bit's level (slot group 7 closes the tree at
+            // level 4)
+            vg = f2_add(g1[i], f2_add(g0[i], vg));
+            vp = f2_add(p1[i], f2_add(p0[i], vp));
+            const int ones = __ffs(~m) - 1;
+            for (int l = 2; l < 2 + ones && l < 5; ++l) {
+                vg = f2_add(lvl(l, 0, i), vg);
+                vp = f2_add(lvl(l, 1, i), vp);
             }
+            const int dst = 2 + ones < 4 ? 2 + ones : 4;
+            lvl(dst, 0, i) = vg;
+            lvl(dst, 1, i) = vp;
         }
-        if (ones < 2) {
-#pragma unroll
-            for (int l = 0; l < 2; ++l) {
-                if (l == ones) {
-                    g[l][i] = vg;
-                    p[l][i] = vp;
-                }
-            }
-            return;
-        }
-        for (int l = 2; l < ones && l < 5; ++l) {
-            vg = f2_add(lvl(l, 0, i), vg);
-            vp = f2_add(lvl(l, 1, i), vp);
-        }
-        const int dst = ones < 4 ? ones : 4;
-        lvl(dst, 0, i) = vg;
-        lvl(dst, 1, i) = vp;
     }
 };
 
@@ -729,8 +725,10 @@ __global__ void __launch_bounds__(32 * (kBwdMaxOutWarps + kBwdStatWarps), 1)
         tr.up = up + t;
         tr.stride = nout;
 #pragma unroll 1
-        for (int k = 0; k < 32; ++k) {
-            const int ones = __ffs(~k) - 1;  // trailing one bits of k
+        for (int m = 0; m < 8; ++m) {
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4) {
+            const int k = 4 * m + i4;
             if (k < nrows) {
                 const uint32_t s = sp.slot;
                 wait(smem_addr(&ready_bar[s]), sp.par);
@@ -775,14 +773,31 @@ __global__ void __launch_bounds__(32 * (kBwdMaxOutWarps + kBwdStatWarps), 1)
                     const float t1 = __fsub_rn(__fsub_rn(d1, st.z), __fmul_rn(y1, st.w));
                     word(o, i) = pack_bf2(__fmul_rn(st.y, t0), __fmul_rn(st.y, t1));
                     // token-tree values: g, and g * R(yhat) (exact: two bf16)
-                    tr.push(ones, i, gf, f2_mul(gf, f2_from_bf2(bf2_from_f2(yhat))));
+                    const u64 gp = f2_mul(gf, f2_from_bf2(bf2_from_f2(yhat)));
+                    if (i4 == 0)
+                        tr.push<0>(m, i, gf, gp);
+                    else if (i4 == 1)
+                        tr.push<1>(m, i, gf, gp);
+                    else if (i4 == 2)
+                        tr.push<2>(m, i, gf, gp);
+                    else
+                        tr.push<3>(m, i, gf, gp);
                 }
                 st_stream(gx + (r0 + k) * Dv + t, o);
             } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    tr.push(ones, i, 0ull, 0ull);  // +0 past the end of the sequence
+                for (int i = 0; i < 4; ++i) {  // +0 past the end of the sequence
+                    if (i4 == 0)
+                        tr.push<0>(m, i, 0ull, 0ull);
+                    else if (i4 == 1)
+                        tr.push<1>(m, i, 0ull, 0ull);
+                    else if (i4 == 2)
+                        tr.push<2>(m, i, 0ull, 0ull);
+                    else
+                        tr.push<3>(m, i, 0ull, 0ull);
+                }
             }
+        }
         }
 
         // the block's values -> workspace [B][nblk][2][D]: quantity 0 =

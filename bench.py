@@ -200,6 +200,8 @@ KERNEL_SOURCES = {
     "row_kernel_ws": ("row_kernels.cu", "device_common.cuh", "launch.h"),
     "qk_kernel": ("qk_kernel.cu", "device_common.cuh", "launch.h"),
     "wan_kernel": ("wan_kernel.cu", "device_common.cuh", "launch.h"),
+    "bwd_ws_kernel": ("backward.cu", "device_common.cuh", "launch.h"),
+    "tokens_top_kernel": ("backward.cu", "device_common.cuh", "launch.h"),
 }
 
 
@@ -407,10 +409,29 @@ def main():
         torch.cuda.synchronize(dev)
         return s0.elapsed_time(s1) / n
 
+    # the same bytes moved by a plain device-to-device copy (x -> out, the
+    # same rotating buffers, timed the same way): the practical ceiling of a
+    # launch this short
+    def copy_back_to_back(which, n=200):
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(PRIME_CYCLES)
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for i in range(n):
+                st = sets[i % nsets]
+                st[2 + which].copy_(st[which])
+            s1.record(stream)
+        torch.cuda.synchronize(dev)
+        return s0.elapsed_time(s1) / n
+
     t1, t2 = back_to_back(0), back_to_back(1)
+    c1, c2 = copy_back_to_back(0), copy_back_to_back(1)
     per_launch = {
-        "ln_modulate_1x4608x3072": {"us": 1e3 * t1, "gbs": b1 / (t1 * 1e-3) / 1e9},
-        "ln_modulate_2x4608x3072": {"us": 1e3 * t2, "gbs": b2 / (t2 * 1e-3) / 1e9},
+        "ln_modulate_1x4608x3072": {"us": 1e3 * t1, "gbs": b1 / (t1 * 1e-3) / 1e9,
+                                    "copy_us": 1e3 * c1, "of_copy_speed": c1 / t1},
+        "ln_modulate_2x4608x3072": {"us": 1e3 * t2, "gbs": b2 / (t2 * 1e-3) / 1e9,
+                                    "copy_us": 1e3 * c2, "of_copy_speed": c2 / t2},
     }
     # DRAM bytes of the average launch (the step is one launch of each shape)
     t_b1 = traffic_record("row_kernel_ws", "ln_modulate_flux_1x4608x3072")

@@ -37,6 +37,38 @@ namespace {
 
 __device__ unsigned int g_error;
 
+// As mbar_try_wait, but the thread may be suspended (up to `hint_ns`) until the
+// phase completes instead of returning at once: waiters take no issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait for waits that are usually long (a consumer behind its
+// producer): suspended waits of up to 20 us each, same overall limit.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity,
+                                                unsigned long long limit_ns)
+{
+    if (mbar_try_wait_sleep(bar, parity, 20000u))
+        return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u))
+            return true;
+        if (global_ns() - t0 > limit_ns)
+            return false;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // grad_x
 // ---------------------------------------------------------------------------

@@ -145,7 +145,9 @@ int ln_modulate_folded(const void* x, const void* scale, const void* shift, void
  *                overwritten, and in use until the call's work on `stream`
  *                is done.
  *   Errors as ln_modulate; RMSMOD_ERR_SHAPE also when workspace_bytes is
- *   too small.  Three kernel launches on `stream`; nothing is allocated.
+ *   too small.  One to three kernel launches on `stream` (two when grad_x
+ *   and a modulation gradient are both wanted, D is a multiple of 256 from
+ *   1024 to 3072 and S >= 2); nothing is allocated.
  * ---------------------------------------------------------------------- */
 size_t ln_modulate_backward_workspace_bytes(int64_t B, int64_t S, int64_t D);
 

@@ -606,7 +606,15 @@ def kernel_table(rm, lib, dev, stream, l2, peak, iters=200, only=None):
             for i in range(5):
                 calls[i % nsets]()
             stream.synchronize()
-            torch.cuda._sleep(PRIME_CYCLES)
+            # the host cost of one call (binding checks, views): the GPU sleep
+            # must outlast queueing all `iters` calls, or the burst would time
+            # the host
+            h0 = time.perf_counter()
+            for i in range(5):
+                calls[i % nsets]()
+            host_s = (time.perf_counter() - h0) / 5
+            stream.synchronize()
+            torch.cuda._sleep(max(PRIME_CYCLES, int(3 * iters * host_s * 2.1e9)))
             s0 = torch.cuda.Event(enable_timing=True)
             s1 = torch.cuda.Event(enable_timing=True)
             s0.record(stream)
@@ -616,7 +624,7 @@ def kernel_table(rm, lib, dev, stream, l2, peak, iters=200, only=None):
         torch.cuda.synchronize(dev)
         per = s0.elapsed_time(s1) / iters
         gbs = bytes_ / (per * 1e-3) / 1e9
-        rows[name] = {"us": per * 1e3, "gbs": gbs, "frac": gbs / peak,
+        rows[name] = {"us": per * 1e3, "gbs": gbs, "frac": gbs / peak, "host_us": host_s * 1e6,
                       "rows_per_s": nrows / (per * 1e-3), "bytes": bytes_, "sets": nsets}
 
     def nsets_for(set_bytes):
@@ -738,10 +746,12 @@ def kernel_table(rm, lib, dev, stream, l2, peak, iters=200, only=None):
         qkvs = [normal((T, 3, H, hd), 2.0) for _ in range(n)]
         wq, bq = normal((hd,), 0.05, 1.0), normal((hd,), 0.02)
         wk, bk = normal((hd,), 0.05, 1.0), normal((hd,), 0.02)
+        views = [(t[:, 0], t[:, 1]) for t in qkvs]
         timed(name, 2 * T * H * hd * 4 + 4 * hd * 2, 2 * T * H,
-              [lambda t=t: rm.qk_layernorm(t[:, 0], t[:, 1], wq, bq, wk, bk, q_out=t[:, 0],
-                                           k_out=t[:, 1], stream=stream)
-               for t in qkvs])
+              [lambda q=q, k=k: rm.qk_layernorm(q, k, wq, bq, wk, bk, q_out=q, k_out=k,
+                                                stream=stream)
+               for q, k in views])
+        del views
         del qkvs
 
     # channels-last RMSNorm + SiLU, Wan VAE

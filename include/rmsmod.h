@@ -331,6 +331,16 @@ int rmsmod_supported(int op, int64_t D_or_C, const void* const* ptrs, int nptrs)
 #define RMSMOD_DEVICE_ERR_COPY_TIMEOUT 1u
 int rmsmod_device_status(unsigned int* bits, int clear);
 
+/* Self-test of that error path (the pages have no counterpart): launches
+ * one warp on `stream` that waits `limit_ns` nanoseconds (1 .. 100,000,000)
+ * on an mbarrier that nothing ever completes, the way every TMA-fed kernel
+ * of this library bounds its waits, then sets RMSMOD_DEVICE_ERR_COPY_TIMEOUT
+ * in the device error word and returns.  No fault, no hang: after the stream
+ * is synchronised, rmsmod_device_status reports the bit and the context
+ * stays usable.  Returns RMSMOD_OK, RMSMOD_ERR_SHAPE (limit out of range,
+ * nothing launched) or RMSMOD_ERR_CUDA. */
+int rmsmod_selftest_wait_timeout(uint64_t limit_ns, rmsmod_stream_t stream);
+
 /* Static text for a status code (never NULL). */
 const char* rmsmod_status_string(int status);
 

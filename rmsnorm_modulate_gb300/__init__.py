@@ -26,6 +26,7 @@ __all__ = [
     "rmsnorm_modulate",
     "gated_rmsnorm_modulate", "qk_layernorm", "rmsnorm_silu_cl", "modulate_scale_shift",
     "residual_gate_add", "conv_bias_epilogue", "supported", "status_string", "device_status",
+    "selftest_wait_timeout",
     "OP_LN_MODULATE", "OP_RMSNORM_MODULATE", "OP_GATED_RMSNORM_MODULATE",
     "OP_QK_LAYERNORM", "OP_RMSNORM_SILU_CL", "OP_LN_MODULATE_FOLDED",
 ]
@@ -86,6 +87,7 @@ def library() -> ctypes.CDLL:
             "rmsmod_status_string": [C],
             "rmsmod_version": [],
             "rmsmod_device_status": [ctypes.POINTER(ctypes.c_uint), C],
+            "rmsmod_selftest_wait_timeout": [ctypes.c_uint64, P],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -487,6 +489,13 @@ def device_status(clear: bool = False) -> int:
     bits = ctypes.c_uint(0)
     _call("rmsmod_device_status", ctypes.byref(bits), 1 if clear else 0)
     return int(bits.value)
+
+
+def selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None) -> None:
+    """Launch the library's bounded-wait self-test: one warp waits `limit_ns`
+    on a barrier nothing completes, then sets bit 0 of the device error word
+    (read it with device_status after synchronising)."""
+    _call("rmsmod_selftest_wait_timeout", int(limit_ns), _stream(stream))
 
 
 def supported(op: int, d_or_c: int, *tensors) -> bool:

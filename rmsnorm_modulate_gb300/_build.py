@@ -18,7 +18,7 @@ LIB = os.path.join(PKG, "librmsmod.so")
 HEADER = os.path.join(ROOT, "include", "rmsmod.h")
 
 SOURCES = ["api.cu", "row_kernels.cu", "qk_kernel.cu", "wan_kernel.cu", "elementwise.cu",
-           "backward.cu"]
+           "backward.cu", "selftest.cu"]
 
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -134,16 +134,24 @@ RMSMOD_EXPORT int rmsmod_device_status(unsigned int* bits, int clear)
 {
     if (!bits)
         return RMSMOD_ERR_NULL;
-    unsigned a = 0, b = 0, c = 0, d = 0;
+    unsigned a = 0, b = 0, c = 0, d = 0, e = 0;
     if (rmsmod::row_kernels_error(&a, clear != 0) != cudaSuccess ||
         rmsmod::qk_kernel_error(&b, clear != 0) != cudaSuccess ||
         rmsmod::wan_kernel_error(&c, clear != 0) != cudaSuccess ||
-        rmsmod::backward_error(&d, clear != 0) != cudaSuccess) {
+        rmsmod::backward_error(&d, clear != 0) != cudaSuccess ||
+        rmsmod::selftest_error(&e, clear != 0) != cudaSuccess) {
         cudaGetLastError();
         return RMSMOD_ERR_CUDA;
     }
-    *bits = a | b | c | d;
+    *bits = a | b | c | d | e;
     return RMSMOD_OK;
+}
+
+RMSMOD_EXPORT int rmsmod_selftest_wait_timeout(uint64_t limit_ns, rmsmod_stream_t stream)
+{
+    if (limit_ns == 0 || limit_ns > 100000000ull)
+        return RMSMOD_ERR_SHAPE;
+    return launch_status(rmsmod::launch_selftest_wait(limit_ns, stream));
 }
 
 static bool qk_head_dim_ok(int64_t hd) { return hd == 64 || hd == 96 || hd == 128; }

@@ -252,9 +252,34 @@ def cpu_baseline(seconds: float):
         oracle.ln_modulate(x, B1["scale"], B1["shift"])
         n += 1
     dt = time.perf_counter() - t0
-    return {"value": per * n / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    line = {"value": per * n / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{n} calls x 64 rows of x[1,4608,3072] (D=3072) through the single-"
                       f"threaded C oracle, {dt:.1f} s"}
+    # the same oracle, row-parallel: one host thread per core, each calling
+    # the (unchanged, single-threaded) C oracle on its own 64-row block of
+    # x[1,4608,3072] (ctypes releases the interpreter lock during the call)
+    from concurrent.futures import ThreadPoolExecutor
+
+    cores = min(len(os.sched_getaffinity(0)), 4608 // 64)
+    blocks = [np.ascontiguousarray(B1["x"][:, 64 * i:64 * (i + 1)]) for i in range(cores)]
+
+    def work(xb):
+        k = 0
+        t_end = time.perf_counter() + seconds / 2
+        while time.perf_counter() < t_end:
+            oracle.ln_modulate(xb, B1["scale"], B1["shift"])
+            k += 1
+        return k
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        calls = sum(ex.map(work, blocks))
+    dt = time.perf_counter() - t0
+    line["row_parallel"] = {
+        "value": per * calls / dt / 1e9, "unit": "GB/s", "cores": cores,
+        "sample": f"{calls} calls x 64 rows on {cores} threads (one 64-row block each), "
+                  f"{dt:.1f} s"}
+    return line
 
 
 def main():
@@ -640,6 +665,43 @@ def kernel_table(rm, lib, dev, stream, l2, peak, iters=200, only=None):
         outs = [torch.empty_like(x) for _ in range(8)]
         timed(name, 256 * 1024 * 4 + 4 * 1024, 256,
               [lambda o=o: rm.ln_modulate(x, sc, sh, out=o, stream=stream) for o in outs])
+    # the same small launch as a CUDA graph of 1000 launches (no host in the
+    # loop): what one launch costs the GPU when nothing else hides it
+    name = "ln_modulate_1x256x1024_graph1000"
+    if want(name):
+        x = normal((1, 256, 1024))
+        sc, sh = normal((1, 1, 1024), 0.1), normal((1, 1, 1024), 0.1)
+        outs = [torch.empty_like(x) for _ in range(8)]
+        cap = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(cap):
+            for o in outs:  # first calls (launch attributes) outside the capture
+                rm.ln_modulate(x, sc, sh, out=o, stream=cap)
+        cap.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        try:
+            with torch.cuda.graph(graph, stream=cap):
+                for i in range(1000):
+                    rm.ln_modulate(x, sc, sh, out=outs[i % 8], stream=cap)
+        except Exception as exc:  # capture refused: report it, keep the table
+            rows[name] = {"error": f"{type(exc).__name__}: {exc}"[:200]}
+            graph = None
+    if want(name) and graph is not None:
+        with torch.cuda.stream(cap):
+            graph.replay()
+            cap.synchronize()
+            torch.cuda._sleep(PRIME_CYCLES)
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record(cap)
+            graph.replay()
+            s1.record(cap)
+        torch.cuda.synchronize(dev)
+        per = s0.elapsed_time(s1) / 1000
+        bytes_ = 256 * 1024 * 4 + 4 * 1024
+        rows[name] = {"us": per * 1e3, "gbs": bytes_ / (per * 1e-3) / 1e9,
+                      "frac": bytes_ / (per * 1e-3) / 1e9 / peak, "launches": 1000,
+                      "rows_per_s": 256 / (per * 1e-3), "bytes": bytes_, "sets": 8}
+        del graph
     for B in (1, 2):
         name = f"ln_modulate_flux_{B}x4608x3072"
         if not want(name):

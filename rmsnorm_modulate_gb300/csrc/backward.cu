@@ -791,19 +791,22 @@ __global__ void __launch_bounds__(32 * (kBwdMaxOutWarps + kBwdStatWarps), 1)
                 sp.advance(1u, ns);
                 ++seq;
                 const u64 mean2 = f2_splat(st.x), rstd2 = f2_splat(st.y);
+                const u64 c1c1 = f2_splat(st.z);
                 uint4 o;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const u64 yhat = f2_mul(f2_sub(f2_from_bf2(word(xv, i)), mean2), rstd2);
                     const u64 gf = f2_from_bf2(word(gv, i));
-                    const u64 dy = f2_mul(gf, f2_from_bf2(word(s1v, i)));
-                    float y0, y1, d0, d1;
+                    // grad_x = R(rstd * ((dyhat - c1) - R32(yhat * c2))).  Packed:
+                    // dyhat = g * s1 is exact (two bf16), so whether it is
+                    // contracted into the subtraction or not, d = RN(dyhat -
+                    // c1); the inexact yhat * c2 is two separately rounded
+                    // products (never contracted)
+                    const u64 d = f2_sub(f2_mul(gf, f2_from_bf2(word(s1v, i))), c1c1);
+                    float y0, y1;
                     f2_unpack(yhat, y0, y1);
-                    f2_unpack(dy, d0, d1);
-                    // grad_x = R(rstd * ((dyhat - c1) - R32(yhat * c2)))
-                    const float t0 = __fsub_rn(__fsub_rn(d0, st.z), __fmul_rn(y0, st.w));
-                    const float t1 = __fsub_rn(__fsub_rn(d1, st.z), __fmul_rn(y1, st.w));
-                    word(o, i) = pack_bf2(__fmul_rn(st.y, t0), __fmul_rn(st.y, t1));
+                    const u64 t = f2_sub(d, f2_pack(__fmul_rn(y0, st.w), __fmul_rn(y1, st.w)));
+                    word(o, i) = bf2_from_f2(f2_mul(rstd2, t));
                     // token-tree values: g, and g * R(yhat) (exact: two bf16)
                     const u64 gp = f2_mul(gf, f2_from_bf2(bf2_from_f2(yhat)));
                     if (i4 == 0)

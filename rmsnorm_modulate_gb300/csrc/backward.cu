@@ -980,11 +980,16 @@ static bool launch_fused(const BwdArgs& a, const DeviceInfo& dev, cudaStream_t s
     const int Wout = a.Dv / 32;
     if (Wout < kBwdMinOutWarps || Wout > kBwdMaxOutWarps)
         return false;
-    // ring slots: as many as ~220 KB hold beside the upper tree levels
+    // ring slots: about 96 KB of rows in multiples of the statistics warps
+    // (8 slots at D = 3072; at that shape 8 measured faster than 6, 10, 12
+    // or 14), within what ~220 KB holds beside the upper tree levels
     constexpr int kBudget = 220 * 1024;
     const int slot_bytes = 2 * a.Dv * 16;
     const int up_bytes = 3 * 8 * 32 * Wout * 8;
-    int nslots = (kBudget - up_bytes) / slot_bytes;
+    int nslots = (96 * 1024 / slot_bytes) / kBwdStatWarps * kBwdStatWarps;
+    nslots = nslots < kBwdStatWarps ? kBwdStatWarps : nslots;
+    const int fit = (kBudget - up_bytes) / slot_bytes;
+    nslots = nslots > fit ? fit : nslots;
     nslots = nslots > kBwdMaxSlots ? kBwdMaxSlots : nslots;
     const int smem = nslots * slot_bytes + up_bytes;
     const int threads = 32 * (Wout + kBwdStatWarps);

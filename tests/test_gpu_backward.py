@@ -66,6 +66,7 @@ def run(rm, oracle_mod, inp, want_exact_rows=0.99):
     (1, 40, 2560, False),   # ten warps
     (2, 1100, 1024, True),  # 35 blocks per batch, two CTAs per SM
     (3, 1700, 3072, True),  # more blocks than CTAs: each CTA loops over several
+    (10, 40, 3072, True),   # more batches' s1 rows than shared memory holds
     # the trees above the first level
     (1, 32768, 8, False),   # 1024 blocks: 32 level-2 nodes, the widest lane groups
     (1, 33000, 8, False),   # 1032 blocks: past the lane groups, one thread per column

@@ -13,18 +13,25 @@
 //   grad_shift = T_s(f(g))                 grad_scale = T_s(f(g) * f(R(yhat)))
 // with T_s the token tree over the S rows of the batch.
 //
-// Three launches:
-//   dx_kernel      one warp per row: x and g rows land in shared memory by
-//                  1-D bulk copies; pass 1 forms c1, c2 as double-float sums
-//                  (TwoSum per value, TwoProd for dyhat * yhat), pass 2
-//                  writes grad_x.
-//   tokens_l1      four lanes per (batch, 32-token block, 4 columns): each
-//                  lane the tree of 8 token slots in registers (a binary
-//                  counter, +0 for slots past the end), two butterfly steps
-//                  for the top levels, both quantities; the block values go
-//                  to the workspace.
-//   tokens_up      one thread per (batch, column): the trees above the first
-//                  level over the block values, completed to 32^L slots.
+// Kernels:
+//   bwd_ws_kernel  grad_x and the first tree level (the value of every
+//                  32-token block) in one pass over x and g: statistics warps
+//                  (c1, c2 per row) and output warps (grad_x, the block
+//                  trees) around a ring of rows fed by 1-D bulk copies.  Used
+//                  when both are wanted, D is a multiple of 256 from 1024 to
+//                  3072 and S >= 2.
+//   dx_kernel      grad_x alone (or at other D): one warp per row, x and g
+//                  rows in shared memory, pass 1 forms c1, c2, pass 2 writes
+//                  grad_x.
+//   tokens_l1      the block values alone (or at other D): four lanes per
+//                  (batch, block, 4 columns), 8 token slots per lane in
+//                  registers, two butterfly steps for the top levels.
+//   tokens_top     the trees above the first level for 2..1024 blocks: one
+//                  lane per level-2 node, lane groups per column.
+//   tokens_up      the same for any number of blocks: one thread per
+//                  (batch, column), completed to 32^L slots.
+// c1 and c2 are double-float sums everywhere (TwoSum per value, TwoProd for
+// dyhat * yhat): the exact sums up to the rounding of the low word.
 #include <cstddef>
 #include <mutex>
 
@@ -482,10 +489,11 @@ __global__ void __launch_bounds__(kTokThreads) tokens_up_kernel(const BwdArgs a)
 //       into the slot's statistics, then the slot's ready barrier
 // Each output warp releases a slot with one atomic add; the last of them
 // refills it with the row nslots further on, after tagging the slot with that
-// row's sequence number.  A statistics warp may reach a slot before the
-// previous fill of it has landed (its rows are not those nslots apart), where
-// the barrier's parity would alias; it checks the tag first.  x and g are
-// read from HBM once.
+// row's sequence number.  Were nslots not a multiple of the statistics warps,
+// a statistics warp could reach a slot before the previous fill of it has
+// landed (its rows would not be nslots apart), where the barrier's parity
+// aliases; the launcher sizes the ring in such multiples, and the warp checks
+// the tag before waiting all the same.  x and g are read from HBM once.
 
 constexpr int kBwdStatWarps = 8;
 constexpr int kBwdMaxOutWarps = 12;  // D <= 3072

@@ -10,6 +10,7 @@
 
 #include "../../include/rmsmod.h"
 #include "launch.h"
+#include "selftest.h"
 
 #define RMSMOD_EXPORT extern "C" __attribute__((visibility("default")))
 

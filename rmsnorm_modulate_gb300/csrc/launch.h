@@ -181,9 +181,5 @@ cudaError_t row_kernels_error(unsigned* bits, bool clear);
 cudaError_t qk_kernel_error(unsigned* bits, bool clear);
 cudaError_t wan_kernel_error(unsigned* bits, bool clear);
 cudaError_t backward_error(unsigned* bits, bool clear);
-cudaError_t selftest_error(unsigned* bits, bool clear);
-
-// One warp waiting `limit_ns` on a barrier nothing completes (selftest.cu).
-cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
 
 }  // namespace rmsmod

@@ -6,6 +6,7 @@
 // usable.
 #include "device_common.cuh"
 #include "launch.h"
+#include "selftest.h"
 
 namespace rmsmod {
 

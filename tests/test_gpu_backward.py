@@ -76,9 +76,11 @@ def test_shapes(rm, oracle_mod, B, S, D, per_batch):
 
 
 def test_flux_full_size(rm, oracle_mod):
+    # every difference must come from a c1 / c2 rounding tie (rare); a fused
+    # multiply-add anywhere in grad_x would leave ~1e-4 of all elements off
     inp = make(1, 4608, 3072, seed=21)
-    d = run(rm, oracle_mod, inp)
-    assert (d == 0).mean() > 0.9999
+    d = run(rm, oracle_mod, inp, want_exact_rows=0.999)
+    assert (d == 0).mean() > 0.99999
 
 
 @pytest.mark.parametrize("need_x", [True, False])

@@ -564,8 +564,9 @@ def main():
         "pct_of_nominal_8tbs": 100.0 * value / world / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "row_kernel_ws<LN, V=12> (ln_modulate, D=3072: 8 statistics + "
-                               "4 output warps around a 16-row TMA ring)",
+                     "kernel": "row_kernel_ws<LN, V=12> (ln_modulate, D=3072: statistics and "
+                               "output warps around a 16-row TMA ring; 4 + 8 warps for the "
+                               "16-row items of B=1, 8 + 4 for the 31-row items of B=2)",
                      "traffic_per": "average launch of the step (B=1 and B=2 shapes)",
                      "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                      "algorithmic_bytes_per_launch": {"B1": b1, "B2": b2}},

@@ -468,12 +468,14 @@ __global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads, RowShape<OP, V
 // ---------------------------------------------------------------------------
 
 // Rows up to 3072 values: 8 statistics + 4 output warps, two CTAs per SM;
-// 4096 values: 8 + 8 warps and one CTA per SM with a 176 KB ring (the
-// epilogue's share of the work grows with the weight row of RMSNorm).
-template <int OP, int V>
+// with SHORT work items (16 rows or fewer per CTA, where the output warps'
+// last rows set the end of the launch) 4 + 8.  4096 values: 8 + 8 warps and
+// one CTA per SM with a 176 KB ring (the epilogue's share of the work grows
+// with the weight row of RMSNorm).
+template <int OP, int V, bool SHORT = false>
 struct WsShape {
-    static constexpr int kStatWarps = 8;
-    static constexpr int kOutWarps = V >= 16 ? 8 : 4;
+    static constexpr int kStatWarps = (V < 16 && SHORT) ? 4 : 8;
+    static constexpr int kOutWarps = (V >= 16 || SHORT) ? 8 : 4;
     static constexpr int kBlocks = V >= 16 ? 1 : 2;
     static constexpr int kRingBudget = (V >= 16 ? 176 : 100) * 1024;
     static constexpr int kWarps = kStatWarps + kOutWarps;
@@ -546,12 +548,12 @@ __device__ __noinline__ void slow_stats_smem(const uint4* buf, int Dv, uint32_t 
     }
 }
 
-template <int OP, int V, bool EXACT>
-__global__ void __launch_bounds__(WsShape<OP, V>::kThreads, WsShape<OP, V>::kBlocks)
+template <int OP, int V, bool EXACT, bool SHORT>
+__global__ void __launch_bounds__(WsShape<OP, V, SHORT>::kThreads, WsShape<OP, V, SHORT>::kBlocks)
     row_kernel_ws(const RowArgs a, const Items items)
 {
     grid_dependency_sync();
-    using Shape = WsShape<OP, V>;
+    using Shape = WsShape<OP, V, SHORT>;
     constexpr int kSlots = Shape::kSlots;
     constexpr int kSegVec = Shape::kSegVec;
     constexpr int kSlotVec = Shape::kSlotVec;
@@ -756,11 +758,11 @@ __global__ void __launch_bounds__(WsShape<OP, V>::kThreads, WsShape<OP, V>::kBlo
         drain_pause();
 }
 
-template <int OP, int V, bool EXACT>
+template <int OP, int V, bool EXACT, bool SHORT>
 cudaError_t launch_ws(const RowArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
-    using Shape = WsShape<OP, V>;
-    auto kern = row_kernel_ws<OP, V, EXACT>;
+    using Shape = WsShape<OP, V, SHORT>;
+    auto kern = row_kernel_ws<OP, V, EXACT, SHORT>;
     constexpr int kSmemMax = Shape::kRingBytes + Shape::kCacheBytes;
     static int blocks_per_sm[64] = {0};
     const int d = dev.device & 63;
@@ -838,9 +840,21 @@ template <int OP, int V, int WPR>
 cudaError_t launch_cfg(const RowArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
     if constexpr (WPR == 1 && (V == 16 || (V == 12 && OP != kOpGated))) {
+        if constexpr (V == 12) {
+            // rows per work item at two CTAs per SM (as launch_ws splits them)
+            const int64_t B = a.rows / a.S;
+            int64_t per_batch = static_cast<int64_t>(dev.sms) * 2 / (B > 0 ? B : 1);
+            const int64_t max_items = (a.S + 7) / 8;
+            per_batch = per_batch > max_items ? max_items : (per_batch < 1 ? 1 : per_batch);
+            if ((a.S + per_batch - 1) / per_batch <= 16) {
+                if (a.Dv == 32 * V)
+                    return launch_ws<OP, V, true, true>(a, dev, stream);
+                return launch_ws<OP, V, false, true>(a, dev, stream);
+            }
+        }
         if (a.Dv == 32 * V)
-            return launch_ws<OP, V, true>(a, dev, stream);
-        return launch_ws<OP, V, false>(a, dev, stream);
+            return launch_ws<OP, V, true, false>(a, dev, stream);
+        return launch_ws<OP, V, false, false>(a, dev, stream);
     }
     if (a.Dv == 32 * V * WPR)
         return launch_shape<OP, V, WPR, true>(a, dev, stream);

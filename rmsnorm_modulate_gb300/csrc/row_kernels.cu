@@ -1,16 +1,22 @@
 // ln_modulate / rmsnorm_modulate / gated_rmsnorm_modulate on sm_103a.
 //
-// One warp (or a group of 2 / 4 warps for D > 4096, each owning a
-// contiguous segment of the row) processes one row at a time and loops
-// persistently over rows.  Rows arrive in shared memory by 1-D bulk copies
-// (TMA, cp.async.bulk) into a two-stage ring per warp, tracked by mbarriers:
-// while a warp computes row k, row k + 1 is already in flight, so HBM sees
-// a continuous stream independent of how long the arithmetic takes.  From
-// shared memory the row goes to registers as packed bf16, the exact
-// statistics are formed, and the normalise + modulate epilogue runs on
-// packed f32x2 / bf16x2 instructions and streams the result out.  HBM is
-// touched once per element in each direction; scale, shift, weight and gate
-// rows are re-read from L1/L2.
+// Two kernels, both fed by 1-D bulk copies (TMA, cp.async.bulk) into shared
+// memory tracked by mbarriers, so HBM sees a continuous stream independent of
+// how long the arithmetic takes:
+//   row_kernel     (D <= 2048, D > 4096, and gated rows up to 3072) one warp (or a
+//                  group of 2 / 4 warps for D > 4096, each owning a contiguous
+//                  segment of the row) processes one row at a time from a
+//                  two-stage ring of its own and loops persistently over rows.
+//   row_kernel_ws  (2048 < D <= 4096) warp-specialised: statistics warps and
+//                  output warps around one ring of row slots per CTA; a
+//                  statistics warp forms a row's mean / rstd and hands the
+//                  slot to the output warps, which normalise, modulate, store
+//                  and refill it.
+// The exact statistics are formed from packed bf16, the normalise + modulate
+// epilogue runs on packed f32x2 / bf16x2 instructions and streams the result
+// out.  HBM is touched once per element in each direction; scale, shift,
+// weight and gate rows are staged once per work item in shared memory (rows
+// of up to 4096 values) or re-read from L1/L2 (longer rows).
 //
 // Arithmetic per element follows the eager chain of the pages:
 //   LayerNorm (sglang #34008 GLM-Image, §What "rounding-faithful" means here):

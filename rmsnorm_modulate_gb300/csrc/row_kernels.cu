@@ -477,13 +477,16 @@ __global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads, RowShape<OP, V
 // with SHORT work items (16 rows or fewer per CTA, where the output warps'
 // last rows set the end of the launch) 4 + 8.  4096 values: 8 + 8 warps and
 // one CTA per SM with a 176 KB ring (the epilogue's share of the work grows
-// with the weight row of RMSNorm).
+// with the weight row of RMSNorm); gated, whose slots hold two rows and
+// whose statistics warps also write the residual stream out, 4 + 12 warps
+// around 12 slots (192 KB).
 template <int OP, int V, bool SHORT = false>
 struct WsShape {
-    static constexpr int kStatWarps = (V < 16 && SHORT) ? 4 : 8;
-    static constexpr int kOutWarps = (V >= 16 || SHORT) ? 8 : 4;
+    static constexpr bool kGatedWide = (V >= 16 && OP == kOpGated);
+    static constexpr int kStatWarps = kGatedWide ? 4 : ((V < 16 && SHORT) ? 4 : 8);
+    static constexpr int kOutWarps = kGatedWide ? 12 : ((V >= 16 || SHORT) ? 8 : 4);
     static constexpr int kBlocks = V >= 16 ? 1 : 2;
-    static constexpr int kRingBudget = (V >= 16 ? 176 : 100) * 1024;
+    static constexpr int kRingBudget = (kGatedWide ? 192 : (V >= 16 ? 176 : 100)) * 1024;
     static constexpr int kWarps = kStatWarps + kOutWarps;
     static constexpr int kThreads = 32 * kWarps;
     static constexpr int kSegVec = 32 * V;
@@ -496,7 +499,8 @@ struct WsShape {
     // which take their rows in order, so no barrier is ever waited on with
     // the parity of a phase two steps ahead (which would read as complete).
     static constexpr int kSlotsRaw = kRingBudget / (kSlotVec * 16);
-    static constexpr int kSlots = kSlotsRaw / kStatWarps * kStatWarps;
+    static constexpr int kSlotStep = kGatedWide ? 12 : kStatWarps;  // a multiple of both
+    static constexpr int kSlots = kSlotsRaw / kSlotStep * kSlotStep;
     static constexpr int kRingBytes = kSlots * kSlotVec * 16;
     static_assert(kSlots >= kStatWarps && kSlots % kStatWarps == 0 && kSlots % kOutWarps == 0,
                   "a slot must return to the same statistics and output warps");

@@ -66,6 +66,36 @@ def dist_env():
     return rank, world, local
 
 
+def timed_over_ranks(pg, device, run):
+    """The timed region of one replica per rank: a barrier on both sides of
+    `run()`, which returns this rank's device-timed milliseconds (with a
+    device synchronise on both sides of its events), then the maximum over
+    the ranks -- the job ends with its slowest replica."""
+    if pg is not None:
+        pg.barrier()
+    ms = run()
+    if pg is not None:
+        pg.barrier()
+        import torch
+
+        t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms
+
+
+def job_throughput(world, units_per_replica, steps, total_ms):
+    """Whole-job throughput: the units every rank processed over the
+    max-over-ranks time (weak scaling: each replica runs the full step)."""
+    return world * units_per_replica * steps / (total_ms * 1e-3)
+
+
+def emit(rank, line):
+    """One JSON line, from rank 0 only."""
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason sampling in the background."""
 
@@ -389,31 +419,26 @@ def main():
     # A short GPU sleep first lets the host queue launches ahead of the GPU,
     # so the K steps run back to back; CUDA events on the launch stream
     # bracket exactly the K steps (the sleep lies before the start event).
-    e_start = torch.cuda.Event(enable_timing=True)
-    e_end = torch.cuda.Event(enable_timing=True)
-    if pg is not None:
-        pg.barrier()
-    torch.cuda.synchronize(dev)
-    sampler.mark("timed_start")
-    with torch.cuda.stream(stream):
-        torch.cuda._sleep(PRIME_CYCLES)
-        e_start.record(stream)
-        for i in range(args.steps):
-            a, b = calls[i % nsets]
-            if f(*a) != 0 or f(*b) != 0:
-                raise RuntimeError("ln_modulate launch failed")
-        e_end.record(stream)
-    torch.cuda.synchronize(dev)
-    sampler.mark("timed_end")
-    if pg is not None:
-        pg.barrier()
-    total_ms = e_start.elapsed_time(e_end)
-    if pg is not None:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    def timed_steps():
+        e_start = torch.cuda.Event(enable_timing=True)
+        e_end = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        sampler.mark("timed_start")
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(PRIME_CYCLES)
+            e_start.record(stream)
+            for i in range(args.steps):
+                a, b = calls[i % nsets]
+                if f(*a) != 0 or f(*b) != 0:
+                    raise RuntimeError("ln_modulate launch failed")
+            e_end.record(stream)
+        torch.cuda.synchronize(dev)
+        sampler.mark("timed_end")
+        return e_start.elapsed_time(e_end)
+
+    total_ms = timed_over_ranks(pg, dev, timed_steps)
     ms_per_step = total_ms / args.steps
-    value = world * step_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    value = job_throughput(world, step_bytes, args.steps, total_ms) / 1e9
     # the dominant (and only) kernel of the step is ln_modulate; its average
     # launch moves step_bytes / 2 in ms_per_step / 2
     achieved = step_bytes / (ms_per_step * 1e-3) / 1e9
@@ -516,27 +541,26 @@ def main():
         for i in range(4):
             e2e_step(i)
         torch.cuda.synchronize(dev)
-        if pg is not None:
-            pg.barrier()
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(s_in):
-            torch.cuda._sleep(PRIME_CYCLES)
-            s0.record(s_in)
-        for i in range(e_steps):
-            e2e_step(i)
-        s_out.wait_event(ev_run[(e_steps - 1) % nset])
-        with torch.cuda.stream(s_out):
-            s1.record(s_out)
-        torch.cuda.synchronize(dev)
-        e_ms = s0.elapsed_time(s1)
-        if pg is not None:
-            t = torch.tensor([e_ms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e_ms = float(t.item())
+
+        def timed_e2e():
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            with torch.cuda.stream(s_in):
+                torch.cuda._sleep(PRIME_CYCLES)
+                s0.record(s_in)
+            for i in range(e_steps):
+                e2e_step(i)
+            s_out.wait_event(ev_run[(e_steps - 1) % nset])
+            with torch.cuda.stream(s_out):
+                s1.record(s_out)
+            torch.cuda.synchronize(dev)
+            return s0.elapsed_time(s1)
+
+        e_ms = timed_over_ranks(pg, dev, timed_e2e)
         h2d = (hx1[0].numel() + hx2[0].numel() + sum(t.numel() for t in hmod[0])) * 2
         d2h = (ho1[0].numel() + ho2[0].numel()) * 2
-        e2e = {"value": world * step_bytes * e_steps / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        e2e = {"value": job_throughput(world, step_bytes, e_steps, e_ms) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
                "ms_per_step": e_ms / e_steps,
                "pipelining": "2 buffer sets, host->device / compute / device->host on 3 streams"}
@@ -548,6 +572,8 @@ def main():
     clocks = ClockSampler.summarise(sampler.stop())
 
     if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
         return 0
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -559,7 +585,7 @@ def main():
                    "l2": f"{nsets} rotating input/output sets, {nsets * set_bytes / 2**20:.0f} "
                          f"MiB > 4x the {l2 / 2**20:.0f} MiB L2",
                    "parallelism": f"replicas x{world}"},
-        "rows_per_s": world * step_rows * args.steps / (total_ms * 1e-3),
+        "rows_per_s": job_throughput(world, step_rows, args.steps, total_ms),
         "pct_of_roofline": 100.0 * value / world / peak,
         "pct_of_nominal_8tbs": 100.0 * value / world / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -577,7 +603,7 @@ def main():
         "cpu_baseline": cpu_baseline(args.cpu_seconds) if world == 1 else None,
         "kernels": kernels,
     }
-    print(json.dumps(line))
+    emit(rank, line)
     if pg is not None:
         pg.destroy_process_group()
     return 0
@@ -650,8 +676,11 @@ def kernel_table(rm, lib, dev, stream, l2, peak, iters=200, only=None):
         torch.cuda.synchronize(dev)
         per = s0.elapsed_time(s1) / iters
         gbs = bytes_ / (per * 1e-3) / 1e9
-        rows[name] = {"us": per * 1e3, "gbs": gbs, "frac": gbs / peak, "host_us": host_s * 1e6,
-                      "rows_per_s": nrows / (per * 1e-3), "bytes": bytes_, "sets": nsets}
+        rows[name] = {"us": per * 1e3, "gbs": gbs, "frac": gbs / peak,
+                      "frac_nominal_8tbs": gbs / NOMINAL_HBM_GBS, "host_us": host_s * 1e6,
+                      "rows_per_s": nrows / (per * 1e-3), "bytes": bytes_, "sets": nsets,
+                      # every buffer the rotation touches fits in L2 (small shapes)
+                      "l2_resident": nsets * bytes_ < l2}
 
     def nsets_for(set_bytes):
         """Enough rotating sets that each launch's buffers were evicted from L2."""
@@ -716,6 +745,62 @@ def kernel_table(rm, lib, dev, stream, l2, peak, iters=200, only=None):
               [lambda a=a, o=o: rm.ln_modulate(a, sc, sh, out=o, stream=stream)
                for a, o in zip(xs, os_)])
         del xs, os_
+
+    # the FLUX.1 text stream (1, 512, 3072): a short launch, L2-resident
+    name = "ln_modulate_flux_text_1x512x3072"
+    if want(name):
+        S, D = 512, 3072
+        n = nsets_for(S * D * 4)
+        xs = [normal((1, S, D)) for _ in range(n)]
+        sc, sh = normal((1, 1, D), 0.1), normal((1, 1, D), 0.1)
+        os_ = [torch.empty_like(xs[0]) for _ in range(n)]
+        timed(name, S * D * 4 + 2 * D * 2, S,
+              [lambda a=a, o=o: rm.ln_modulate(a, sc, sh, out=o, stream=stream)
+               for a, o in zip(xs, os_)])
+        del xs, os_
+
+    # the standalone elementwise chains: FLUX.1's modulate at the image and
+    # text stream shapes (bf16 and fp16), ERNIE-Image's residual gate, the
+    # Wan VAE conv-bias epilogue with and without the residual h
+    for S in (4608, 512):
+        for dt, tag in ((torch.bfloat16, "bf16"), (torch.float16, "f16")):
+            name = f"modulate_scale_shift_{tag}_1x{S}x3072"
+            if not want(name):
+                continue
+            D = 3072
+            n = nsets_for(S * D * 4)
+            ys = [normal((1, S, D), dtype=dt) for _ in range(n)]
+            sc, sh = normal((1, 1, D), 0.1, dtype=dt), normal((1, 1, D), 0.1, dtype=dt)
+            os_ = [torch.empty_like(ys[0]) for _ in range(n)]
+            timed(name, S * D * 4 + 2 * D * 2, S,
+                  [lambda a=a, o=o: rm.modulate_scale_shift(a, sc, sh, out=o, stream=stream)
+                   for a, o in zip(ys, os_)])
+            del ys, os_
+    name = "residual_gate_add_1x4216x4096"
+    if want(name):
+        S, D = 4216, 4096
+        n = nsets_for(S * D * 6)
+        rs_in = [normal((1, S, D)) for _ in range(n)]
+        us = [normal((1, S, D)) for _ in range(n)]
+        gate = normal((1, 1, D), 0.1)
+        os_ = [torch.empty_like(rs_in[0]) for _ in range(n)]
+        timed(name, S * D * 6 + D * 2, S,
+              [lambda a=a, u=u, o=o: rm.residual_gate_add(a, gate, u, out=o, stream=stream)
+               for a, u, o in zip(rs_in, us, os_)])
+        del rs_in, us, os_
+    for with_h in (False, True):
+        C = 96
+        name = f"conv_bias_epilogue{'_residual' if with_h else ''}_wan_c{C}"
+        if not want(name):
+            continue
+        npx = W.WAN_PIXELS
+        xw = normal((npx, C))
+        hw = normal((npx, C)) if with_h else None
+        bias = normal((C,), 0.1, dtype=torch.float32)
+        ow = torch.empty_like(xw)
+        timed(name, npx * C * (6 if with_h else 4) + C * 4, npx,
+              [lambda: rm.conv_bias_epilogue(xw, bias, hw, out=ow, stream=stream)])
+        del xw, hw, ow
 
     # the single-rounding tier on the CFG pair
     name = "ln_modulate_folded_flux_2x4608x3072"

@@ -135,9 +135,12 @@ int ln_modulate_folded(const void* x, const void* scale, const void* shift, void
  *
  *   x, grad_out  bf16 [B*S*D];  scale bf16 rows at base + b * mod_bstride
  *   mean, rstd   fp32 [B*S], the forward's
- *   grad_x       nullable bf16 [B*S*D] (must not overlap any input)
+ *   grad_x       nullable bf16 [B*S*D]
  *   grad_scale, grad_shift  nullable fp32 [B, D] (one row per batch; with a
  *                shared modulation row the caller sums the rows over b)
+ *   No output (grad_x, grad_scale, grad_shift, workspace) may overlap an
+ *   input (x, grad_out, the scale rows, mean, rstd) or another output:
+ *   RMSMOD_ERR_UNSUPPORTED, nothing launched.
  *   workspace    device memory of at least
  *                ln_modulate_backward_workspace_bytes(B, S, D) bytes,
  *                256-byte aligned; needed when grad_scale or grad_shift is
@@ -161,9 +164,15 @@ int ln_modulate_backward(const void* x, const void* scale, int64_t mod_bstride,
  * ln_modulate_backward_static -- ln_modulate_backward without a caller
  * workspace.  The pages have no counterpart: this is a library convenience.
  *
+ *   For callers that cannot hand the library device memory: a host
+ *   framework whose own allocator owns the device and exposes no buffer to
+ *   plug-ins, or a latency-critical path that must not call cudaMalloc
+ *   (which can synchronise the whole device) between steps.
  *   Same arguments, results and errors as ln_modulate_backward minus the
  *   workspace: the token-sum scratch is a fixed 8 MiB (8 << 20 bytes) array
- *   of the library's own device memory, so the call allocates nothing.
+ *   of the library's own device memory, so the call allocates nothing
+ *   (every GPU that loads the library holds those 8 MiB until the process
+ *   exits).
  *   Sizes whose ln_modulate_backward_workspace_bytes(B, S, D) exceeds
  *   8 MiB return RMSMOD_ERR_SHAPE and launch nothing (grad_x alone needs no
  *   scratch and has no such limit).  Nothing in the scratch needs clearing:

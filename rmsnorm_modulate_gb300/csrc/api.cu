@@ -283,12 +283,21 @@ RMSMOD_EXPORT int ln_modulate_backward(const void* x, const void* scale, int64_t
         return RMSMOD_ERR_SHAPE;
     const int64_t bytes = tensor_bytes(rows, D);
     const int64_t col_bytes = B * D * 4;
-    // outputs overlap no input and no other output (grad_x may not alias x)
-    const void* ins[] = {x, grad_out};
-    for (const void* in : ins)
-        if (overlap(grad_x, bytes, in, bytes) || overlap(grad_scale, col_bytes, in, bytes) ||
-            overlap(grad_shift, col_bytes, in, bytes) ||
-            (tokens && overlap(workspace, static_cast<int64_t>(need), in, bytes)))
+    // the scale rows the kernels read: row b at scale + b * mod_bstride
+    const int64_t scale_bytes = ((B - 1) * mod_bstride + D) * 2;
+    // outputs overlap no input and no other output (grad_x may not alias x):
+    // the kernels write grad_x, the workspace and the gradients while other
+    // CTAs still read x, grad_out, scale, mean and rstd
+    struct Span {
+        const void* p;
+        int64_t n;
+    };
+    const Span ins[] = {{x, bytes}, {grad_out, bytes}, {scale, scale_bytes},
+                        {mean, 4 * rows}, {rstd, 4 * rows}};
+    for (const Span& in : ins)
+        if (overlap(grad_x, bytes, in.p, in.n) || overlap(grad_scale, col_bytes, in.p, in.n) ||
+            overlap(grad_shift, col_bytes, in.p, in.n) ||
+            (tokens && overlap(workspace, static_cast<int64_t>(need), in.p, in.n)))
             return RMSMOD_ERR_UNSUPPORTED;
     if (overlap(grad_x, bytes, grad_scale, col_bytes) ||
         overlap(grad_x, bytes, grad_shift, col_bytes) ||

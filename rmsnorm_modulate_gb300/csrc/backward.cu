@@ -82,6 +82,7 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity,
 
 constexpr int kDxMaxWarps = 8;
 constexpr int kDxThreads = 32 * kDxMaxWarps;  // upper bound; long rows use fewer warps
+constexpr int kDxSmemMax = 200 * 1024;         // shared memory of one dx_kernel CTA, at most
 
 // (hi, lo) += v, exactly up to the rounding of lo (TwoSum).
 __device__ __forceinline__ void dd_acc(u64& hi, u64& lo, u64 v)
@@ -931,8 +932,10 @@ static __device__ __align__(256) unsigned char g_backward_scratch[kBackwardScrat
 cudaError_t backward_static_scratch(int device, void** ptr)
 {
     static std::mutex mu;
-    static void* addr[64] = {nullptr};
-    const int d = device & 63;
+    static void* addr[kMaxDevices] = {nullptr};
+    if (device < 0 || device >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    const int d = device;
     std::lock_guard<std::mutex> lock(mu);
     if (!addr[d]) {
         // once per device (loads the module's device data if needed)
@@ -1001,15 +1004,15 @@ static bool launch_fused(const BwdArgs& a, const DeviceInfo& dev, cudaStream_t s
     nslots = nslots > kBwdMaxSlots ? kBwdMaxSlots : nslots;
     const int smem = nslots * slot_bytes + up_bytes;
     const int threads = 32 * (Wout + kBwdStatWarps);
-    static bool configured[64] = {false};
-    const int d = dev.device & 63;
-    if (!configured[d]) {
-        e = cudaFuncSetAttribute(bwd_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kBudget);
-        if (e != cudaSuccess)
-            return true;
-        configured[d] = true;
-    }
+    static PerDeviceInt configured;
+    int done = 0;
+    e = configured.get(dev.device, done, [&](int& v) -> cudaError_t {
+        v = 1;
+        return cudaFuncSetAttribute(bwd_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kBudget);
+    });
+    if (e != cudaSuccess)
+        return true;
     const int64_t items = a.B * a.nblk;
     const int64_t cap = dev.sms;  // one CTA per SM
     e = launch_dependent(bwd_ws_kernel, static_cast<int>(items < cap ? items : cap), threads,
@@ -1029,18 +1032,19 @@ cudaError_t launch_backward(BwdArgs a, const DeviceInfo& dev, cudaStream_t strea
         // warps per CTA: as many as ~200 KB of shared memory hold (x and g
         // rows per warp plus the s1 row), at most eight
         const int row_vec = a.Dv;
-        int warps = (200 * 1024 / 16 - row_vec) / (2 * row_vec);
+        int warps = (kDxSmemMax / 16 - row_vec) / (2 * row_vec);
         warps = warps > kDxMaxWarps ? kDxMaxWarps : (warps < 1 ? 1 : warps);
         const int smem = (row_vec + warps * 2 * row_vec) * 16;
-        static int configured[64] = {0};
-        const int d = dev.device & 63;
-        if (configured[d] < smem) {
-            e = cudaFuncSetAttribute(dx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     smem);
-            if (e != cudaSuccess)
-                return e;
-            configured[d] = smem;
-        }
+        // the kernel's largest dynamic shared memory (~200 KB), set once per device
+        static PerDeviceInt configured;
+        int done = 0;
+        e = configured.get(dev.device, done, [&](int& v) -> cudaError_t {
+            v = 1;
+            return cudaFuncSetAttribute(dx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kDxSmemMax);
+        });
+        if (e != cudaSuccess)
+            return e;
         int nb = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, dx_kernel, 32 * warps, smem);
         if (e != cudaSuccess)

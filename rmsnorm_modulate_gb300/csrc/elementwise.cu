@@ -99,19 +99,24 @@ __global__ void __launch_bounds__(kThreads)
 template <int OP>
 cudaError_t launch(const EwArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
-    static int blocks_per_sm[64] = {0};
-    const int d = dev.device & 63;
-    if (blocks_per_sm[d] == 0) {
-        int nb = 0;
-        cudaError_t e =
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, ew_kernel<OP>, kThreads, 0);
-        if (e != cudaSuccess)
-            return e;
-        blocks_per_sm[d] = nb > 0 ? nb : 1;
+    static PerDeviceInt blocks_per_sm;
+    int bps = 0;
+    {
+        const cudaError_t e0 = blocks_per_sm.get(dev.device, bps, [&](int& v) -> cudaError_t {
+            int nb = 0;
+            cudaError_t e =
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, ew_kernel<OP>, kThreads, 0);
+            if (e != cudaSuccess)
+                return e;
+            v = nb > 0 ? nb : 1;
+            return cudaSuccess;
+        });
+        if (e0 != cudaSuccess)
+            return e0;
     }
     const uint32_t total = static_cast<uint32_t>(a.rows * a.Dv);
     const int64_t want = (static_cast<int64_t>(total) + kThreads * kIlp - 1) / (kThreads * kIlp);
-    const int64_t cap = static_cast<int64_t>(dev.sms) * blocks_per_sm[d];
+    const int64_t cap = static_cast<int64_t>(dev.sms) * bps;
     const int grid = static_cast<int>(want < cap ? want : cap);
     const FastDiv fd_row = FastDiv::make(static_cast<uint32_t>(a.Dv));
     const FastDiv fd_batch = FastDiv::make(static_cast<uint32_t>(a.S > 0 ? a.S : 1));

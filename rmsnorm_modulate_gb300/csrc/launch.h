@@ -2,14 +2,53 @@
 // translation units.  Internal to librmsmod.so.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 namespace rmsmod {
 
+// Devices the library serves: the C ABI refuses a current device ordinal
+// outside [0, kMaxDevices) before anything is launched.
+constexpr int kMaxDevices = 64;
+
 struct DeviceInfo {
-    int device;
+    int device;  // in [0, kMaxDevices)
     int sms;
+};
+
+// One int per device, worked out by the first call on that device (a kernel
+// attribute set, an occupancy query) and read by every later call.  Host
+// threads whose first calls coincide serialise on one mutex, so the set-up
+// runs once per device and a reader never sees a half-written value.
+class PerDeviceInt {
+public:
+    // value for `device`; `make(int& v)` computes it (non-zero) on first use
+    template <typename F>
+    cudaError_t get(int device, int& value, F make)
+    {
+        if (device < 0 || device >= kMaxDevices)
+            return cudaErrorInvalidDevice;
+        int v = v_[device].load(std::memory_order_acquire);
+        if (v == 0) {
+            std::lock_guard<std::mutex> lock(mu_);
+            v = v_[device].load(std::memory_order_relaxed);
+            if (v == 0) {
+                const cudaError_t e = make(v);
+                if (e != cudaSuccess)
+                    return e;
+                v = v != 0 ? v : 1;
+                v_[device].store(v, std::memory_order_release);
+            }
+        }
+        value = v;
+        return cudaSuccess;
+    }
+
+private:
+    std::atomic<int> v_[kMaxDevices] = {};
+    std::mutex mu_;
 };
 
 // Integer division by a runtime constant: q = (umulhi(n, m) + n) >> s,

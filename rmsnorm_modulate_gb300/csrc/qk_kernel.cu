@@ -328,25 +328,30 @@ cudaError_t launch_ws(const QkArgs& a, const DeviceInfo& dev, cudaStream_t strea
     using Shape = QkShape<RV, P>;
     auto kern = qk_kernel_ws<RV, P>;
     constexpr int kSmem = kWsSlots * Shape::kTileVec * 16;
-    static int blocks_per_sm[64] = {0};
-    const int d = dev.device & 63;
-    if (blocks_per_sm[d] == 0) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (e != cudaSuccess)
-            return e;
-        int nb = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kWsThreads, kSmem);
-        if (e != cudaSuccess)
-            return e;
-        blocks_per_sm[d] = nb > 0 ? nb : 1;
+    static PerDeviceInt blocks_per_sm;
+    int bps = 0;
+    {
+        const cudaError_t e0 = blocks_per_sm.get(dev.device, bps, [&](int& v) -> cudaError_t {
+            cudaError_t e =
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+            if (e != cudaSuccess)
+                return e;
+            int nb = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kWsThreads, kSmem);
+            if (e != cudaSuccess)
+                return e;
+            v = nb > 0 ? nb : 1;
+            return cudaSuccess;
+        });
+        if (e0 != cudaSuccess)
+            return e0;
     }
     auto tiles_of = [](const QkTensor& t) {
         return t.tokens * ((t.heads + Shape::kTileRows - 1) / Shape::kTileRows);
     };
     const int64_t tq = tiles_of(a.t[0]), tk = tiles_of(a.t[1]);
     const int64_t total = tq + tk;
-    const int64_t cap = static_cast<int64_t>(dev.sms) * blocks_per_sm[d];
+    const int64_t cap = static_cast<int64_t>(dev.sms) * bps;
     int64_t bq, bk;
     if (tq + tk <= cap) {
         bq = tq;

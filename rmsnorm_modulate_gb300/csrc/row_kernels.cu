@@ -774,20 +774,25 @@ cudaError_t launch_ws(const RowArgs& a, const DeviceInfo& dev, cudaStream_t stre
     using Shape = WsShape<OP, V, SHORT>;
     auto kern = row_kernel_ws<OP, V, EXACT, SHORT>;
     constexpr int kSmemMax = Shape::kRingBytes + Shape::kCacheBytes;
-    static int blocks_per_sm[64] = {0};
-    const int d = dev.device & 63;
-    if (blocks_per_sm[d] == 0) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-        if (e != cudaSuccess)
-            return e;
-        int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Shape::kThreads, kSmemMax);
-        if (e != cudaSuccess)
-            return e;
-        blocks_per_sm[d] = n > 0 ? n : 1;
+    static PerDeviceInt blocks_per_sm;
+    int bps = 0;
+    {
+        const cudaError_t e0 = blocks_per_sm.get(dev.device, bps, [&](int& v) -> cudaError_t {
+            cudaError_t e =
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+            if (e != cudaSuccess)
+                return e;
+            int n = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Shape::kThreads, kSmemMax);
+            if (e != cudaSuccess)
+                return e;
+            v = n > 0 ? n : 1;
+            return cudaSuccess;
+        });
+        if (e0 != cudaSuccess)
+            return e0;
     }
-    const int64_t cap = static_cast<int64_t>(dev.sms) * blocks_per_sm[d];
+    const int64_t cap = static_cast<int64_t>(dev.sms) * bps;
     const int64_t B = a.rows / a.S;
     int64_t per_batch = cap / (B > 0 ? B : 1);
     const int64_t max_items = (a.S + Shape::kStatWarps - 1) / Shape::kStatWarps;
@@ -810,21 +815,26 @@ cudaError_t launch_shape(const RowArgs& a, const DeviceInfo& dev, cudaStream_t s
     using Shape = RowShape<OP, V, WPR>;
     auto kern = row_kernel<OP, V, WPR, EXACT>;
     constexpr int kSmemMax = Shape::kRingBytes + Shape::kCacheBytes;
-    static int blocks_per_sm[64] = {0};
-    const int d = dev.device & 63;
-    if (blocks_per_sm[d] == 0) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-        if (e != cudaSuccess)
-            return e;
-        int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Shape::kThreads, kSmemMax);
-        if (e != cudaSuccess)
-            return e;
-        blocks_per_sm[d] = n > 0 ? n : 1;
+    static PerDeviceInt blocks_per_sm;
+    int bps = 0;
+    {
+        const cudaError_t e0 = blocks_per_sm.get(dev.device, bps, [&](int& v) -> cudaError_t {
+            cudaError_t e =
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+            if (e != cudaSuccess)
+                return e;
+            int n = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, Shape::kThreads, kSmemMax);
+            if (e != cudaSuccess)
+                return e;
+            v = n > 0 ? n : 1;
+            return cudaSuccess;
+        });
+        if (e0 != cudaSuccess)
+            return e0;
     }
     constexpr int kGroups = Shape::kWarps / WPR;
-    const int64_t cap = static_cast<int64_t>(dev.sms) * blocks_per_sm[d];
+    const int64_t cap = static_cast<int64_t>(dev.sms) * bps;
     const int64_t B = a.rows / a.S;
     // split each batch into enough items to fill the GPU, each item at least
     // one row per group when the rows allow it

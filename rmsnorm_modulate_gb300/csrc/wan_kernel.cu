@@ -288,23 +288,28 @@ cudaError_t launch_shape(const WanArgs& a, const DeviceInfo& dev, cudaStream_t s
 {
     auto kern = wan_kernel<P, V, EXACT>;
     constexpr int kSmemMax = WanShape<V>::kRingBytes + 2 * kMaxCv * 16;
-    static int blocks_per_sm[64] = {0};
-    const int d = dev.device & 63;
-    if (blocks_per_sm[d] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemMax);
-        if (e != cudaSuccess)
-            return e;
-        int nb = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads,
-                                                          WanShape<V>::kRingBytes + 2 * a.Cv * 16);
-        if (e != cudaSuccess)
-            return e;
-        blocks_per_sm[d] = nb > 0 ? nb : 1;
+    static PerDeviceInt blocks_per_sm;
+    int bps = 0;
+    {
+        const cudaError_t e0 = blocks_per_sm.get(dev.device, bps, [&](int& v) -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kSmemMax);
+            if (e != cudaSuccess)
+                return e;
+            int nb = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads,
+                                                              WanShape<V>::kRingBytes + 2 * a.Cv * 16);
+            if (e != cudaSuccess)
+                return e;
+            v = nb > 0 ? nb : 1;
+            return cudaSuccess;
+        });
+        if (e0 != cudaSuccess)
+            return e0;
     }
     constexpr int kPixPerBlock = (32 / P) * kWarps;
     const int64_t want = (a.pixels + kPixPerBlock - 1) / kPixPerBlock;
-    const int64_t cap = static_cast<int64_t>(dev.sms) * blocks_per_sm[d];
+    const int64_t cap = static_cast<int64_t>(dev.sms) * bps;
     const int grid = static_cast<int>(want < cap ? want : cap);
     const int smem = WanShape<V>::kRingBytes + 2 * a.Cv * 16;
     return launch_dependent(kern, grid, kThreads, smem, stream, a);

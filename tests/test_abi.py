@@ -100,6 +100,21 @@ def test_backward_validation_and_workspace_size(lib):
     assert f(*args(gx=X)) == ERR_UNSUPPORTED               # grad_x may not alias x
     assert f(*args(w=GX)) == ERR_UNSUPPORTED               # workspace overlaps grad_x
     assert f(*args(gx=0, gs=0, gh=0)) == OK                # nothing requested: no work
+    # outputs written while other CTAs still read scale, mean and rstd: any
+    # overlap with those inputs is refused, not raced on (the scale rows sit
+    # apart from x here, so each case overlaps exactly one input)
+    SC2 = A + (8 << 24)
+    assert f(*args(sc=SC2, w=SC2)) == ERR_UNSUPPORTED      # workspace over the scale row
+    assert f(*args(w=M)) == ERR_UNSUPPORTED                # workspace over mean
+    assert f(*args(w=R - 256)) == ERR_UNSUPPORTED          # workspace reaching into rstd
+    assert f(*args(sc=SC2, gs=SC2)) == ERR_UNSUPPORTED     # grad_scale over the scale row
+    assert f(*args(sc=SC2, gh=SC2 + 64)) == ERR_UNSUPPORTED  # grad_shift inside the scale row
+    assert f(*args(gh=M + 64)) == ERR_UNSUPPORTED          # grad_shift inside mean
+    assert f(*args(gs=R)) == ERR_UNSUPPORTED               # grad_scale over rstd
+    assert f(*args(gx=M)) == ERR_UNSUPPORTED               # grad_x over mean
+    assert f(*args(gx=R - 16)) == ERR_UNSUPPORTED          # grad_x reaching into rstd
+    # per-batch scale rows: the span reaches the last batch's row
+    assert f(*args(B=2, bs=4096, sc=SC2, gs=SC2 + 2 * 4096)) == ERR_UNSUPPORTED
 
 
 def test_ln_modulate_folded_validation(lib):

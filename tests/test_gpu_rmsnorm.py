@@ -76,6 +76,13 @@ def test_rms_shapes(rm, oracle_mod, B, S, D, with_w, per_batch):
     (1, 64, 8, True, False),
     (2, 31, 40, True, True),
     (1, 70, 4096, True, False),
+    # the 4096-value ring (4 + 12 warps, 12 two-row slots) wrapping many
+    # times, per-batch gate and modulation rows
+    (2, 600, 4096, True, True),
+    (1, 2000, 4096, False, False),
+    # rows of 3080..4088 values: the same ring with a bounds-checked tail
+    (1, 300, 3584, True, False),
+    (2, 257, 4088, True, True),
     (2, 9, 8192, False, True),
 ])
 def test_gated_shapes(rm, oracle_mod, B, S, D, with_w, per_batch):
@@ -108,6 +115,34 @@ def test_rms_edge_and_special_rows(rm, oracle_mod):
             torch.cuda.synchronize()
             o_out, o_rstd = oracle_mod.rmsnorm_modulate(inp["x"], inp["weight"], inp["scale"],
                                                         inp["shift"], 1e-6)
+            g = host(rstd)
+            for i, l in enumerate(labels):
+                assert g[i] == o_rstd[i] or (np.isnan(g[i]) and np.isnan(o_rstd[i])), (D, l)
+            assert_within_ulp(host(out), o_out)
+            assert_exact_where_stats_match(host(out), o_out, D, (g, o_rstd), min_match=0)
+
+
+def test_gated_edge_and_special_rows(rm, oracle_mod):
+    # outlier and non-finite rows through the gated kernels' slow statistics:
+    # the rows are the residual, the update is zero, so the residual stream
+    # equals the rows exactly
+    for D in (64, 3584, 4096):
+        for rows, labels in (W.edge_rows(D), W.special_rows(D)):
+            S = len(labels)
+            inp = W.gated_inputs(1, S, D, seed=3)
+            inp["residual"] = rows.reshape(1, S, D)
+            inp["update"] = np.zeros((1, S, D), np.uint16)
+            rstd = torch.empty(S, dtype=torch.float32, device="cuda")
+            res, out = rm.gated_rmsnorm_modulate(dev(inp["residual"]), dev(inp["update"]),
+                                                 dev(inp["gate"]), dev(inp["weight"]),
+                                                 dev(inp["scale"]), dev(inp["shift"]), 1e-6,
+                                                 rstd_out=rstd)
+            torch.cuda.synchronize()
+            o_res, o_out, o_rstd = oracle_mod.gated_rmsnorm_modulate(
+                inp["residual"], inp["update"], inp["gate"], inp["weight"], inp["scale"],
+                inp["shift"], 1e-6)
+            # bit-exact, NaN payloads aside
+            assert_within_ulp(host(res), o_res, max_ulp=0, frac_1ulp=1.0, what="res")
             g = host(rstd)
             for i, l in enumerate(labels):
                 assert g[i] == o_rstd[i] or (np.isnan(g[i]) and np.isnan(o_rstd[i])), (D, l)

@@ -44,23 +44,46 @@ def test_channels(rm, oracle_mod, C, bias):
     assert np.array_equal(g, o)
 
 
+def oracle_rows_parallel(oracle_mod, x, bias, gamma, eps, block=16384):
+    """The unchanged single-threaded oracle over consecutive blocks of pixel
+    rows, one block per call, on every host core (ctypes releases the
+    interpreter lock during each call); the results are the oracle's own,
+    row for row."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    pixels, C = x.shape
+    out = np.empty_like(x)
+    rstd = np.empty(pixels, np.float32)
+
+    def work(r0):
+        r1 = min(pixels, r0 + block)
+        o, r = oracle_mod.rmsnorm_silu_cl(x[r0:r1], bias, gamma, eps)
+        out[r0:r1] = o
+        rstd[r0:r1] = r
+
+    with ThreadPoolExecutor(max_workers=max(1, len(os.sched_getaffinity(0)))) as ex:
+        list(ex.map(work, range(0, pixels, block)))
+    return out, rstd
+
+
 @pytest.mark.parametrize("C", [96, 192, 384])
-def test_wan_full_size_sampled(rm, oracle_mod, C):
-    """The full [1, C, 4, 480, 832] activation on the GPU; the oracle checks a
-    sample of 20000 pixel rows spread over the whole tensor."""
+def test_wan_full_size(rm, oracle_mod, C):
+    """The full [1, C, 4, 480, 832] activation, every pixel row compared with
+    the oracle: output within 1 ulp everywhere (>= 99.9% of elements at most
+    1 ulp, the standard bar) and every rstd bit-identical."""
     inp = W.WORKLOADS[f"rmsnorm_silu_cl_wan_c{C}"].make()
     pixels = inp["pixels"]
     x = dev(inp["x"])
     rstd = torch.empty(pixels, dtype=torch.float32, device="cuda")
     out = rm.rmsnorm_silu_cl(x, dev(inp["bias"]), dev(inp["gamma"]), 1e-6, rstd_out=rstd)
     torch.cuda.synchronize()
-    idx = np.unique(np.concatenate([np.random.default_rng(C).integers(0, pixels, 20000),
-                                    [0, pixels - 1]]))
-    o_out, o_rstd = oracle_mod.rmsnorm_silu_cl(np.ascontiguousarray(inp["x"][idx]), inp["bias"],
-                                               inp["gamma"], 1e-6)
-    got = host(out[torch.from_numpy(idx).cuda()])
-    assert_within_ulp(got, o_out, max_ulp=1)
-    assert np.array_equal(host(rstd)[idx], o_rstd)
+    got, got_rstd = host(out), host(rstd)
+    del out, x, rstd
+    o_out, o_rstd = oracle_rows_parallel(oracle_mod, inp["x"], inp["bias"], inp["gamma"], 1e-6)
+    assert got.shape == o_out.shape == (pixels, C)
+    assert_within_ulp(got, o_out, max_ulp=1, what=f"Wan C={C} full tensor")
+    assert np.array_equal(got_rstd, o_rstd)
 
 
 def test_channels_last_5d_view(rm, oracle_mod):

@@ -1,8 +1,12 @@
-"""ln_modulate_backward_static (the entry point that uses the library's fixed
-device scratch instead of a caller workspace) against ln_modulate_backward:
-two calls in a row on different inputs must each give bit-identical results
-to the workspace entry point; sizes beyond the fixed scratch are refused.
-Collected last on purpose, and independent of what ran before it."""
+"""ln_modulate_backward_static: the backward entry point for callers that
+cannot give the library device memory (a framework whose allocator owns the
+device, a hot path that must not call cudaMalloc), which uses the library's
+fixed device scratch instead of a caller workspace.  Three calls in a row on
+different inputs, largest first so that later calls meet stale scratch, must
+each give bit-identical results to the workspace entry point; a call changes
+neither torch's allocations nor the device's free memory; sizes beyond the
+fixed scratch are refused.  Collected last on purpose, and independent of
+what ran before it."""
 import ctypes
 
 import numpy as np
@@ -41,7 +45,11 @@ def outputs(B, S, D):
 
 
 def test_two_calls_in_a_row_match_the_workspace_entry_point(rm):
-    cases = [(2, 1100, 256, 31), (1, 4608, 3072, 32)]
+    # the largest case first, so the later calls (other B, S not a multiple
+    # of 32, other D; the one-pass kernel, then the separate token kernels at
+    # D = 256) find stale values of the first in the scratch: nothing they
+    # read may depend on them
+    cases = [(2, 4608, 3072, 32), (3, 1100, 1024, 31), (1, 700, 256, 30)]
     data = [inputs(rm, B, S, D, seed) for B, S, D, seed in cases]
     outs = [outputs(B, S, D) for B, S, D, _ in cases]
     # back to back on one stream, the second reusing the scratch the first wrote
@@ -54,6 +62,26 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point(rm):
         assert torch.equal(gx.view(torch.int16), rx.view(torch.int16))
         assert torch.equal(gsc.view(torch.int32), rsc.view(torch.int32))
         assert torch.equal(gsh.view(torch.int32), rsh.view(torch.int32))
+
+
+def test_a_call_allocates_no_device_memory(rm):
+    B, S, D = 1, 333, 3072
+    x, sc, go, m, r = inputs(rm, B, S, D, 7)
+    gx, gsc, gsh = outputs(B, S, D)
+    rm.ln_modulate_backward_static(x, sc, go, m, r, gx, gsc, gsh)   # set-up call
+    torch.cuda.synchronize()
+    torch_before = torch.cuda.memory_allocated()
+    free_before, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        rm.ln_modulate_backward_static(x, sc, go, m, r, gx, gsc, gsh)
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_allocated() == torch_before
+    assert free_after == free_before
+    rx, rsc, rsh = rm.ln_modulate_backward(x, sc, go, m, r)
+    torch.cuda.synchronize()
+    assert torch.equal(gx.view(torch.int16), rx.view(torch.int16))
+    assert torch.equal(gsc.view(torch.int32), rsc.view(torch.int32))
 
 
 def test_sizes_beyond_the_fixed_scratch_are_refused(rm):

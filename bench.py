@@ -593,7 +593,9 @@ def main():
                      "kernel": "row_kernel_ws<LN, V=12> (ln_modulate, D=3072: statistics and "
                                "output warps around a 16-row TMA ring; 4 + 8 warps for the "
                                "16-row items of B=1, 8 + 4 for the 31-row items of B=2)",
-                     "traffic_per": "average launch of the step (B=1 and B=2 shapes)",
+                     "traffic_per": "average launch of the step (B=1 and B=2 shapes), steady "
+                                    "state: mean of 8 back-to-back launches per shape, each "
+                                    "carrying the previous launch's L2 write-back",
                      "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                      "algorithmic_bytes_per_launch": {"B1": b1, "B2": b2}},
         "per_launch": per_launch,

@@ -42,10 +42,16 @@ struct Log2Ceil<1> {
     static constexpr int value = 0;
 };
 
+// Three CTAs (24 warps) per SM: the per-pixel reduction, rstd and SiLU are
+// chains of dependent instructions, and more resident warps hide them
+// better than deeper rings (the 80-register cap this implies costs no
+// spills).  Tiles in flight per warp: 2 of up to 3 KB (V = 6), 4 below.
+constexpr int kBlocksPerSm = 3;
+
 template <int V>
 struct WanShape {
     static constexpr int kTileVec = 32 * V;  // tile capacity in 16-byte vectors
-    static constexpr int kStages = V >= 6 ? 4 : 6;
+    static constexpr int kStages = V >= 6 ? 2 : 4;
     static constexpr int kRingBytes = kWarps * kStages * kTileVec * 16;
 };
 
@@ -85,7 +91,7 @@ __device__ __forceinline__ u64 silu2_fast(u64 z)
 
 // EXACT: C == 8 * P * V, so no channel vector needs a bounds check.
 template <int P, int V, bool EXACT>
-__global__ void __launch_bounds__(kThreads, 2) wan_kernel(const WanArgs a)
+__global__ void __launch_bounds__(kThreads, kBlocksPerSm) wan_kernel(const WanArgs a)
 {
     grid_dependency_sync();
     constexpr int kL = Log2Ceil<8 * V>::value;

@@ -398,9 +398,12 @@ __device__ __forceinline__ void dd_div_n(float hi, float lo, float n, float inv_
 // rounding is ~2^-48 relative.  acc - K is exact (Sterbenz).  The f32x2
 // registers keep two independent accumulators (even / odd elements).
 //
-// Lanes whose largest magnitude is outside [2^-40, 2^40) or non-finite make
-// the whole row take a slow path (scaled to unit magnitude, or plain IEEE
-// sums that propagate Inf / NaN like the oracle's double sums).
+// The offsets follow a bound on the lane's (or the whole row's) largest
+// magnitude; where that magnitude is outside [2^-40, 2^40) or non-finite the
+// row takes a slow path (scaled to unit magnitude, or plain IEEE sums that
+// propagate Inf / NaN like the oracle's double sums).  Any bound at or above
+// the largest magnitude keeps the sums exact; a looser one moves more of each
+// value into the error terms, whose own fp32 rounding then weighs more.
 
 // The fast range keeps n * sum x^2 and (sum x)^2 (n <= 2^14) far from fp32
 // overflow and every Fast2Sum error term far from the subnormal range.

@@ -232,6 +232,28 @@ KERNEL_SOURCES = {
     "wan_kernel": ("wan_kernel.cu", "device_common.cuh", "launch.h"),
     "bwd_ws_kernel": ("backward.cu", "device_common.cuh", "launch.h"),
     "tokens_top_kernel": ("backward.cu", "device_common.cuh", "launch.h"),
+    "ew_kernel": ("elementwise.cu", "device_common.cuh", "launch.h"),
+}
+
+
+# the dominant kernel of each per-entry-point table row (for its traffic record)
+ROW_KERNEL = {
+    "ln_modulate_flux_1x4608x3072": "row_kernel_ws",
+    "ln_modulate_flux_2x4608x3072": "row_kernel_ws",
+    "rmsnorm_modulate_1x4216x4096": "row_kernel_ws",
+    "gated_rmsnorm_modulate_1x4216x4096": "row_kernel_ws",
+    "ln_modulate_folded_flux_2x4608x3072": "row_kernel_ws",
+    "qk_layernorm_1x4352x32x128": "qk_kernel",
+    "qk_layernorm_qkv_strided_1x4352x32x128": "qk_kernel",
+    "rmsnorm_silu_cl_wan_c96": "wan_kernel",
+    "rmsnorm_silu_cl_wan_c192": "wan_kernel",
+    "rmsnorm_silu_cl_wan_c384": "wan_kernel",
+    "modulate_scale_shift_bf16_1x4608x3072": "ew_kernel",
+    "modulate_scale_shift_f16_1x4608x3072": "ew_kernel",
+    "residual_gate_add_1x4216x4096": "ew_kernel",
+    "conv_bias_epilogue_wan_c96": "ew_kernel",
+    "conv_bias_epilogue_residual_wan_c96": "ew_kernel",
+    "ln_modulate_backward_flux_1x4608x3072": "bwd_ws_kernel",
 }
 
 
@@ -683,6 +705,12 @@ def kernel_table(rm, lib, dev, stream, l2, peak, iters=200, only=None):
                       "rows_per_s": nrows / (per * 1e-3), "bytes": bytes_, "sets": nsets,
                       # every buffer the rotation touches fits in L2 (small shapes)
                       "l2_resident": nsets * bytes_ < l2}
+        kern = ROW_KERNEL.get(name)
+        if kern is not None:
+            # steady-state DRAM bytes per launch from the committed ncu table
+            # (only while the kernel's sources match the recorded digest)
+            rows[name]["traffic"] = traffic_record(kern, name)
+            rows[name]["traffic_kernel"] = kern
 
     def nsets_for(set_bytes):
         """Enough rotating sets that each launch's buffers were evicted from L2."""

@@ -427,6 +427,7 @@ def main():
     sampler.start()
 
     # ---- warm-up (plus a short untimed ramp so clocks settle) ------------
+    torch.cuda.synchronize(dev)  # the input sets were copied on the default stream
     with torch.cuda.stream(stream):
         t_ramp = time.time()
         i = 0
@@ -678,6 +679,11 @@ def kernel_table(rm, lib, dev, stream, l2, peak, iters=200, only=None):
         """Launches back to back after a GPU sleep (the host runs ahead), timed
         as a burst by two events; per launch = burst / launches."""
         nsets = len(calls)
+        # the inputs were drawn on the default stream; the launches run on
+        # `stream`: finish the draws first (an in-place row would otherwise
+        # race its own inputs, and a row that read an unfinished buffer keeps
+        # whatever it wrote)
+        torch.cuda.synchronize(dev)
         with torch.cuda.stream(stream):
             for i in range(5):
                 calls[i % nsets]()
@@ -694,14 +700,19 @@ def kernel_table(rm, lib, dev, stream, l2, peak, iters=200, only=None):
             s0 = torch.cuda.Event(enable_timing=True)
             s1 = torch.cuda.Event(enable_timing=True)
             s0.record(stream)
+            q0 = time.perf_counter()
             for i in range(iters):
                 calls[i % nsets]()
+            queue_s = (time.perf_counter() - q0) / iters
             s1.record(stream)
         torch.cuda.synchronize(dev)
         per = s0.elapsed_time(s1) / iters
         gbs = bytes_ / (per * 1e-3) / 1e9
         rows[name] = {"us": per * 1e3, "gbs": gbs, "frac": gbs / peak,
                       "frac_nominal_8tbs": gbs / NOMINAL_HBM_GBS, "host_us": host_s * 1e6,
+                      # host time per call while queueing the burst: well below
+                      # "us" means the launches ran back to back on the GPU
+                      "host_queue_us": queue_s * 1e6,
                       "rows_per_s": nrows / (per * 1e-3), "bytes": bytes_, "sets": nsets,
                       # every buffer the rotation touches fits in L2 (small shapes)
                       "l2_resident": nsets * bytes_ < l2}
@@ -733,6 +744,7 @@ def kernel_table(rm, lib, dev, stream, l2, peak, iters=200, only=None):
         sc, sh = normal((1, 1, 1024), 0.1), normal((1, 1, 1024), 0.1)
         outs = [torch.empty_like(x) for _ in range(8)]
         cap = torch.cuda.Stream(device=dev)
+        torch.cuda.synchronize(dev)  # inputs drawn on the default stream
         with torch.cuda.stream(cap):
             for o in outs:  # first calls (launch attributes) outside the capture
                 rm.ln_modulate(x, sc, sh, out=o, stream=cap)

@@ -150,7 +150,8 @@ static_assert(kWsSlots % kWsStatWarps == 0 && kWsSlots % kWsOutWarps == 0,
               "a slot must return to the same warps");
 
 template <int RV, int P>
-__global__ void __launch_bounds__(kWsThreads, 2) qk_kernel_ws(const QkArgs a, int blocks_q)
+__global__ void __launch_bounds__(kWsThreads, 2)
+    qk_kernel_ws(const QkArgs a, int blocks_q, FastDiv chunks_q, FastDiv chunks_k)
 {
     grid_dependency_sync();
     using Shape = QkShape<RV, P>;
@@ -175,11 +176,15 @@ __global__ void __launch_bounds__(kWsThreads, 2) qk_kernel_ws(const QkArgs a, in
     const int64_t in_tv = t.in_ts / 8, out_tv = t.out_ts / 8;
     const bool one_token = t.tokens == 1;
     const bool small = tiles < (int64_t(1) << 32);
+    // tile -> token: a multiply-shift division by the tiles per token (the
+    // hardware has no integer divide; a plain division costs ~20 instructions
+    // per tile, a sizeable share of a 16-row tile's statistics)
+    const FastDiv cdiv = is_q ? chunks_q : chunks_k;
     auto token_of = [&](int64_t tile) -> int64_t {
         if (one_token)
             return 0;
         if (small)
-            return static_cast<uint32_t>(tile) / static_cast<uint32_t>(chunks);
+            return cdiv.div(static_cast<uint32_t>(tile));
         return tile / chunks;
     };
     // this CTA's tiles: blk, blk + nblk, ...
@@ -365,7 +370,13 @@ cudaError_t launch_ws(const QkArgs& a, const DeviceInfo& dev, cudaStream_t strea
         bk = cap - bq;
     }
     const int grid = static_cast<int>(bq + bk);
-    return launch_dependent(kern, grid, kWsThreads, kSmem, stream, a, static_cast<int>(bq));
+    // tiles per token of q and of k (at least 1; used only when it fits 32 bits)
+    auto chunks_of = [](const QkTensor& t) {
+        const int64_t c = (t.heads + Shape::kTileRows - 1) / Shape::kTileRows;
+        return FastDiv::make(static_cast<uint32_t>(c > 0 && c < (int64_t(1) << 31) ? c : 1));
+    };
+    return launch_dependent(kern, grid, kWsThreads, kSmem, stream, a, static_cast<int>(bq),
+                            chunks_of(a.t[0]), chunks_of(a.t[1]));
 }
 
 }  // namespace

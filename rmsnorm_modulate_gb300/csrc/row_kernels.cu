@@ -558,52 +558,6 @@ __device__ __noinline__ void slow_stats_smem(const uint4* buf, int Dv, uint32_t 
     }
 }
 
-// Exponent guess of a statistics warp's first rows (|x| < 8): rows of unit
-// scale pass with it, larger ones take one more pass with their own exponent.
-constexpr uint32_t kGuessE0 = 127u + 2u;
-// A guess may exceed a row's exponent by this much before the row takes a
-// second pass (a larger offset moves more of each value into the error
-// terms, whose fp32 rounding then weighs more).
-constexpr uint32_t kGuessSlack = 2u;
-
-// One statistics pass over a row in its slot `buf`: the gated op's residual
-// stream first (RES: written out to `res` and over the residual in the slot),
-// each lane's abs-max, and the exact sums against the offsets of exponent E.
-// E is a guess, valid for the row when its abs-max turns out below
-// 2^(E - 126); the caller checks.
-template <int OP, int V, bool EXACT, bool RES, int kSegVec>
-__device__ __forceinline__ void stats_pass(uint4* buf, uint4* res, const uint4* c_g, int Dv,
-                                           int lane, uint32_t E,
-                                           ExactSums<OP == kOpLN || OP == kOpLNFold>& acc,
-                                           uint32_t& m)
-{
-    constexpr int kL = Log2Ceil<8 * V>::value;
-    acc.init(offset_k1<kL>(E), offset_k2<kL>(E));
-    m = 0;
-#pragma unroll 4
-    for (int j = 0; j < V; ++j) {
-        const int v = j * 32 + lane;
-        if (EXACT || v < Dv) {
-            uint4 xv = buf[v];
-            if (OP == kOpGated && RES) {
-                // the residual stream res = R(residual + R(gate * update)):
-                // written out, and over the residual in the slot for the
-                // output warp (and a second pass)
-                const uint4 u = buf[kSegVec + v], g = c_g[v];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    word(xv, i) = bf2_add(word(xv, i), bf2_mul(word(g, i), word(u, i)));
-                buf[v] = xv;
-                st_stream(res + v, xv);
-            }
-            m = bf2_absmax(m, bf2_absmax(bf2_absmax(xv.x, xv.y), bf2_absmax(xv.z, xv.w)));
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                acc.add(f2_from_bf2(word(xv, i)));
-        }
-    }
-}
-
 template <int OP, int V, bool EXACT, bool SHORT>
 __global__ void __launch_bounds__(WsShape<OP, V, SHORT>::kThreads, WsShape<OP, V, SHORT>::kBlocks)
     row_kernel_ws(const RowArgs a, const Items items)
@@ -687,7 +641,7 @@ __global__ void __launch_bounds__(WsShape<OP, V, SHORT>::kThreads, WsShape<OP, V
             }
         };
 
-        // the first rows of every statistics warp now; the rest of the ring
+        // the first row of every statistics warp now; the rest of the ring
         // once those have landed, so the first rows arrive as early as they can
         if (threadIdx.x == 0)
             for (int64_t r = 0; r < kStatWarps && r < nrows; ++r)
@@ -703,47 +657,69 @@ __global__ void __launch_bounds__(WsShape<OP, V, SHORT>::kThreads, WsShape<OP, V
         __syncthreads();
 
         if (warp < kStatWarps) {
-            // ---- statistics warps: rows warp, warp + kStatWarps, ...  One
-            // pass over a row forms its abs-max and its exact sums against
-            // the offsets of a guessed exponent Eg (the largest exponent of
-            // this warp's previous row, plus one); a row the guess does not
-            // fit takes a second pass with its own exponent.
-            uint32_t Eg = kGuessE0;
+            // ---- statistics warps
             for (int64_t r = warp; r < nrows; r += kStatWarps) {
                 const int s = slot_of(r);
                 wait(smem_addr(&full_bar[s]), parity_of(r));
                 if (r + kStatWarps < kSlots && lane == 0)
                     issue(r + kStatWarps);  // the ring's second half, once
                 uint4* buf = ring + s * kSlotVec;
-                ExactSums<kNeedSum> acc;
-                uint32_t m;
-                stats_pass<OP, V, EXACT, true, kSegVec>(buf, res_out + (r_begin + r) * Dv, c_g,
-                                                        Dv, lane, Eg, acc, m);
+                uint32_t m = 0;
+#pragma unroll
+                for (int j = 0; j < V; ++j) {
+                    const int v = j * 32 + lane;
+                    if (EXACT || v < Dv) {
+                        uint4 xv = buf[v];
+                        if (OP == kOpGated) {
+                            // the residual stream res = R(residual + R(gate * update)):
+                            // written out, and over the residual in the slot for
+                            // the statistics and the output warp
+                            const uint4 u = buf[kSegVec + v], g = c_g[v];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                word(xv, i) = bf2_add(word(xv, i), bf2_mul(word(g, i), word(u, i)));
+                            buf[v] = xv;
+                            st_stream(res_out + (r_begin + r) * Dv + v, xv);
+                        }
+                        m = bf2_absmax(m, bf2_absmax(bf2_absmax(xv.x, xv.y),
+                                                     bf2_absmax(xv.z, xv.w)));
+                    }
+                }
                 if (OP == kOpGated)
                     fence_proxy_async();  // res written over the slot, which the
                                           // async proxy refills later
-                const uint32_t rowmax = __reduce_max_sync(kFullMask, absmax_bits(m));
-                const uint32_t Et = offset_exponent(rowmax);
-                const uint32_t cls = static_cast<uint32_t>(magnitude_class(rowmax));
+                const uint32_t mm = absmax_bits(m);
+                const uint32_t E = offset_exponent(mm);
+                ExactSums<kNeedSum> acc;
+                acc.init(offset_k1<kL>(E), offset_k2<kL>(E));
+#pragma unroll 4
+                for (int j = 0; j < V; ++j) {
+                    const int v = j * 32 + lane;
+                    if (EXACT || v < Dv) {
+                        const uint4 xv = buf[v];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            acc.add(f2_from_bf2(word(xv, i)));
+                    }
+                }
+                float s1h, s1l, s2h, s2l;
+                acc.lane_total(s1h, s1l, s2h, s2l);
+                if (kNeedSum)
+                    dd2_allreduce<32>(s1h, s1l, s2h, s2l);
+                else
+                    dd_allreduce<32>(s2h, s2l);
+                const uint32_t cls =
+                    __reduce_max_sync(kFullMask, static_cast<uint32_t>(magnitude_class(mm)));
+                const uint32_t emax = __reduce_max_sync(kFullMask, mm == 0 ? 0u : (mm >> 7));
                 float mean = 0.0f, stat;
                 if (cls == kClassFast) {
-                    if (!(Et <= Eg && Et + kGuessSlack >= Eg))
-                        stats_pass<OP, V, EXACT, false, kSegVec>(buf, buf, c_g, Dv, lane, Et,
-                                                                 acc, m);
-                    float s1h, s1l, s2h, s2l;
-                    acc.lane_total(s1h, s1l, s2h, s2l);
-                    if (kNeedSum) {
-                        dd2_allreduce<32>(s1h, s1l, s2h, s2l);
+                    if (kNeedSum)
                         finalize_ln(s1h, s1l, s2h, s2l, a.n, a.inv_n, mean, stat);
-                    } else {
-                        dd_allreduce<32>(s2h, s2l);
+                    else
                         stat = finalize_ms(s2h, s2l, a.n, a.inv_n);
-                    }
-                    Eg = Et + 1u < kMaxFastExp ? Et + 1u : kMaxFastExp;
                 } else {
-                    slow_stats_smem<kNeedSum, V, kL, EXACT>(buf, Dv, cls,
-                                                            rowmax == 0 ? 0u : (rowmax >> 7),
-                                                            lane, a.n, a.inv_n, mean, stat);
+                    slow_stats_smem<kNeedSum, V, kL, EXACT>(buf, Dv, cls, emax, lane, a.n,
+                                                            a.inv_n, mean, stat);
                 }
                 const float rstd = rstd_from(stat, a.eps);
                 if (lane == 0) {

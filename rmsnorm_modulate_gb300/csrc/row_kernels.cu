@@ -464,9 +464,10 @@ __global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads, RowShape<OP, V
 // ---------------------------------------------------------------------------
 // Warp-specialised variant for one warp per row (LN / RMS / folded LN,
 // 2048 < D <= 4096).  The CTA owns a ring of kSlots row buffers fed by 1-D
-// bulk copies.  Statistics warps take rows in turn and stream them from
-// shared memory (abs-max, exact sums, butterfly, finalisation, rstd), leave
-// mean / rstd beside the row and arrive on the slot's "ready" barrier;
+// bulk copies.  Statistics warps take rows in turn, read a row from shared
+// memory once into registers (its abs-max on the way), then run the exact
+// sums, butterfly, finalisation and rstd from registers, leave mean / rstd
+// beside the row and arrive on the slot's "ready" barrier;
 // output warps wait for it, normalise + modulate the row from the same
 // buffer, store it, and refill the slot with the row kSlots ahead.  The
 // latency-bound reductions of some rows thus overlap the FMA-bound epilogue
@@ -479,7 +480,9 @@ __global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads, RowShape<OP, V
 // one CTA per SM with a 176 KB ring (the epilogue's share of the work grows
 // with the weight row of RMSNorm); gated, whose slots hold two rows and
 // whose statistics warps also write the residual stream out, 4 + 12 warps
-// around 12 slots (192 KB).
+// around 12 slots (192 KB).  At 4096 values two output warps share each row
+// (half of its vectors each; the later of the two refills the slot), which
+// halves the epilogue latency of a CTA's last rows.
 template <int OP, int V, bool SHORT = false>
 struct WsShape {
     static constexpr bool kGatedWide = (V >= 16 && OP == kOpGated);
@@ -487,6 +490,9 @@ struct WsShape {
     static constexpr int kOutWarps = kGatedWide ? 12 : ((V >= 16 || SHORT) ? 8 : 4);
     static constexpr int kBlocks = V >= 16 ? 1 : 2;
     static constexpr int kRingBudget = (kGatedWide ? 192 : (V >= 16 ? 176 : 100)) * 1024;
+    static constexpr int kOutGroup = V >= 16 ? 2 : 1;  // output warps sharing one row
+    static constexpr int kOutGroups = kOutWarps / kOutGroup;
+    static_assert(kOutWarps % kOutGroup == 0 && V % kOutGroup == 0, "output groups");
     static constexpr int kWarps = kStatWarps + kOutWarps;
     static constexpr int kThreads = 32 * kWarps;
     static constexpr int kSegVec = 32 * V;
@@ -502,7 +508,7 @@ struct WsShape {
     static constexpr int kSlotStep = kGatedWide ? 12 : kStatWarps;  // a multiple of both
     static constexpr int kSlots = kSlotsRaw / kSlotStep * kSlotStep;
     static constexpr int kRingBytes = kSlots * kSlotVec * 16;
-    static_assert(kSlots >= kStatWarps && kSlots % kStatWarps == 0 && kSlots % kOutWarps == 0,
+    static_assert(kSlots >= kStatWarps && kSlots % kStatWarps == 0 && kSlots % kOutGroups == 0,
                   "a slot must return to the same statistics and output warps");
 };
 
@@ -558,6 +564,19 @@ __device__ __noinline__ void slow_stats_smem(const uint4* buf, int Dv, uint32_t 
     }
 }
 
+// One arrival on a shared-memory counter, ordered after this thread's
+// earlier shared-memory reads (acquire-release at CTA scope); returns the
+// count before it.
+__device__ __forceinline__ uint32_t release_add_smem(uint32_t addr)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                 : "=r"(old)
+                 : "r"(addr)
+                 : "memory");
+    return old;
+}
+
 template <int OP, int V, bool EXACT, bool SHORT>
 __global__ void __launch_bounds__(WsShape<OP, V, SHORT>::kThreads, WsShape<OP, V, SHORT>::kBlocks)
     row_kernel_ws(const RowArgs a, const Items items)
@@ -568,7 +587,6 @@ __global__ void __launch_bounds__(WsShape<OP, V, SHORT>::kThreads, WsShape<OP, V
     constexpr int kSegVec = Shape::kSegVec;
     constexpr int kSlotVec = Shape::kSlotVec;
     constexpr int kStatWarps = Shape::kStatWarps;
-    constexpr int kOutWarps = Shape::kOutWarps;
     constexpr int kL = Log2Ceil<8 * V>::value;
     constexpr bool kNeedSum = (OP == kOpLN || OP == kOpLNFold);
     constexpr bool kWeighted = (OP == kOpRMS || OP == kOpGated);
@@ -576,6 +594,7 @@ __global__ void __launch_bounds__(WsShape<OP, V, SHORT>::kThreads, WsShape<OP, V
     extern __shared__ __align__(128) uint4 ring[];
     __shared__ __align__(8) unsigned long long full_bar[kSlots], ready_bar[kSlots];
     __shared__ float2 slot_stats[kSlots];  // (mean, rstd) of the row in each slot
+    __shared__ uint32_t consumed[kSlots];  // output-warp releases of each slot, cumulative
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -602,6 +621,7 @@ __global__ void __launch_bounds__(WsShape<OP, V, SHORT>::kThreads, WsShape<OP, V
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(smem_addr(&full_bar[s]), 1u);
             mbar_init(smem_addr(&ready_bar[s]), 1u);
+            consumed[s] = 0u;
         }
         mbar_init_fence();
     }
@@ -665,9 +685,11 @@ __global__ void __launch_bounds__(WsShape<OP, V, SHORT>::kThreads, WsShape<OP, V
                     issue(r + kStatWarps);  // the ring's second half, once
                 uint4* buf = ring + s * kSlotVec;
                 uint32_t m = 0;
+                uint4 xr[V];  // the lane's vectors, for the sums pass
 #pragma unroll
                 for (int j = 0; j < V; ++j) {
                     const int v = j * 32 + lane;
+                    xr[j] = make_uint4(0u, 0u, 0u, 0u);
                     if (EXACT || v < Dv) {
                         uint4 xv = buf[v];
                         if (OP == kOpGated) {
@@ -681,6 +703,7 @@ __global__ void __launch_bounds__(WsShape<OP, V, SHORT>::kThreads, WsShape<OP, V
                             buf[v] = xv;
                             st_stream(res_out + (r_begin + r) * Dv + v, xv);
                         }
+                        xr[j] = xv;
                         m = bf2_absmax(m, bf2_absmax(bf2_absmax(xv.x, xv.y),
                                                      bf2_absmax(xv.z, xv.w)));
                     }
@@ -692,14 +715,13 @@ __global__ void __launch_bounds__(WsShape<OP, V, SHORT>::kThreads, WsShape<OP, V
                 const uint32_t E = offset_exponent(mm);
                 ExactSums<kNeedSum> acc;
                 acc.init(offset_k1<kL>(E), offset_k2<kL>(E));
-#pragma unroll 4
+#pragma unroll
                 for (int j = 0; j < V; ++j) {
                     const int v = j * 32 + lane;
                     if (EXACT || v < Dv) {
-                        const uint4 xv = buf[v];
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
-                            acc.add(f2_from_bf2(word(xv, i)));
+                            acc.add(f2_from_bf2(word(xr[j], i)));
                     }
                 }
                 float s1h, s1l, s2h, s2l;
@@ -736,15 +758,18 @@ __global__ void __launch_bounds__(WsShape<OP, V, SHORT>::kThreads, WsShape<OP, V
         } else {
             // ---- output warps
             const int ow = warp - kStatWarps;
-            for (int64_t r = ow; r < nrows; r += kOutWarps) {
+            constexpr int kG = Shape::kOutGroup;
+            constexpr int kVG = V / kG;
+            const int grp = ow / kG, q = ow - grp * kG;
+            for (int64_t r = grp; r < nrows; r += Shape::kOutGroups) {
                 const int s = slot_of(r);
                 wait(smem_addr(&ready_bar[s]), parity_of(r));
                 const float2 st = slot_stats[s];
                 const uint4* buf = ring + s * kSlotVec;
                 const int64_t base = (r_begin + r) * Dv;
                 const u64 mean2 = f2_splat(st.x), rstd2 = f2_splat(st.y);
-#pragma unroll 4
-                for (int j = 0; j < V; ++j) {
+#pragma unroll
+                for (int j = q * kVG; j < (q + 1) * kVG; ++j) {
                     const int v = j * 32 + lane;
                     if (EXACT || v < Dv) {
                         const uint4 w =
@@ -754,11 +779,20 @@ __global__ void __launch_bounds__(WsShape<OP, V, SHORT>::kThreads, WsShape<OP, V
                                                                          has_w));
                     }
                 }
-                // the slot is consumed (its statistics warp finished reading
-                // before it arrived): refill it with the row kSlots ahead
+                // this warp's part of the slot is consumed (its statistics
+                // warp finished reading before it arrived); the last warp of
+                // the group to finish refills it with the row kSlots ahead
                 __syncwarp();
-                if (lane == 0)
-                    issue(r + kSlots);
+                if (lane == 0) {
+                    if constexpr (kG == 1) {
+                        issue(r + kSlots);
+                    } else {
+                        const uint32_t old = release_add_smem(smem_addr(&consumed[s]));
+                        const uint32_t round = static_cast<uint32_t>((uses + r) / kSlots);
+                        if (old + 1u == static_cast<uint32_t>(kG) * (round + 1u))
+                            issue(r + kSlots);
+                    }
+                }
             }
         }
         uses += nrows;

@@ -915,12 +915,178 @@ cudaError_t launch_cfg(const RowArgs& a, const DeviceInfo& dev, cudaStream_t str
     return launch_shape<OP, V, WPR, false>(a, dev, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Few rows (a latency-bound launch): one CTA of kCoopWarps warps per row, V
+// 16-byte vectors per lane (D = 1024 V).  A row's statistics then take V
+// vectors of exact sums per lane, a warp butterfly and a combine over the
+// CTA's warps, and nothing waits on a ring; used for at most kCoopRowsPerSm
+// rows per SM, when every row gets a resident CTA at once.  EARLY: the
+// modulation vectors are loaded before the statistics (their latency hidden
+// behind them) instead of after (fewer registers).  Each thread reads its own
+// vectors before it writes them, so out may alias x (and res_out residual).
+// ---------------------------------------------------------------------------
+constexpr int kCoopWarps = 4;
+constexpr int64_t kCoopRowsPerSm = 4;
+
+template <int OP, int V, bool EARLY>
+__global__ void __launch_bounds__(32 * kCoopWarps) row_kernel_coop(const RowArgs a)
+{
+    grid_dependency_sync();
+    constexpr int WPR = kCoopWarps;
+    constexpr bool kNeedSum = (OP == kOpLN || OP == kOpLNFold);
+    constexpr int kL = Log2Ceil<8 * V>::value;
+    __shared__ Slot slots[2][WPR];   // the fast path's exchange, by row parity
+    __shared__ Slot slow_slots[WPR];  // the rare slow path's own exchange
+
+    const int lane = threadIdx.x & 31;
+    const int wig = threadIdx.x >> 5;
+    const int Dv = a.Dv;
+    const uint4* __restrict__ src = static_cast<const uint4*>(OP == kOpGated ? a.residual : a.x);
+    const uint4* __restrict__ upd = static_cast<const uint4*>(a.update);
+    const uint4* __restrict__ gate = static_cast<const uint4*>(a.gate);
+    const uint4* __restrict__ weight = static_cast<const uint4*>(a.weight);
+    const uint4* __restrict__ scale = static_cast<const uint4*>(a.scale);
+    const uint4* __restrict__ shift = static_cast<const uint4*>(a.shift);
+    uint4* __restrict__ res_out = static_cast<uint4*>(a.res_out);
+    uint4* __restrict__ out = static_cast<uint4*>(a.out);
+    const bool has_w = (weight != nullptr);
+    int par = 0;
+    for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x, par ^= 1) {
+        const int64_t b = row / a.S;
+        const int64_t base = row * Dv;
+        uint4 xv[V];
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+            xv[j] = ld_stream(src + base + j * 32 * WPR + threadIdx.x);
+        if (OP == kOpGated) {
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                const int v = j * 32 * WPR + threadIdx.x;
+                const uint4 u = ld_stream(upd + base + v);
+                const uint4 g = ld_cached(gate + b * a.gate_bstride + v);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    word(xv[j], i) = bf2_add(word(xv[j], i), bf2_mul(word(g, i), word(u, i)));
+                st_stream(res_out + base + v, xv[j]);
+            }
+        }
+        uint4 s1[V], h[V], w[V];
+        auto load_mod = [&]() {
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                const int v = j * 32 * WPR + threadIdx.x;
+                s1[j] = ld_cached(scale + b * a.mod_bstride + v);
+                h[j] = ld_cached(shift + b * a.mod_bstride + v);
+                w[j] = (OP == kOpRMS || OP == kOpGated) && has_w ? ld_cached(weight + v)
+                                                                 : make_uint4(0u, 0u, 0u, 0u);
+            }
+        };
+        if (EARLY)
+            load_mod();
+        const uint32_t mm = tree_absmax<V>(xv);
+        const uint32_t E = offset_exponent(mm);
+        ExactSums<kNeedSum> acc;
+        acc.init(offset_k1<kL>(E), offset_k2<kL>(E));
+#pragma unroll
+        for (int j = 0; j < V; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                acc.add(f2_from_bf2(word(xv[j], i)));
+        float s1h, s1l, s2h, s2l;
+        acc.lane_total(s1h, s1l, s2h, s2l);
+        if (kNeedSum)
+            dd2_allreduce<32>(s1h, s1l, s2h, s2l);
+        else
+            dd_allreduce<32>(s2h, s2l);
+        uint32_t cls = __reduce_max_sync(kFullMask, static_cast<uint32_t>(magnitude_class(mm)));
+        uint32_t emax = __reduce_max_sync(kFullMask, mm == 0 ? 0u : (mm >> 7));
+        group_combine<WPR>(&slots[par][0], wig, lane, 0, s1h, s1l, s2h, s2l, cls, emax);
+        float mean = 0.0f, stat;
+        if (cls == kClassFast) {
+            if (kNeedSum)
+                finalize_ln(s1h, s1l, s2h, s2l, a.n, a.inv_n, mean, stat);
+            else
+                stat = finalize_ms(s2h, s2l, a.n, a.inv_n);
+        } else {
+            slow_stats<kNeedSum, V, WPR, kL>(xv, cls, emax, slow_slots, wig, lane, 0, a.n, a.inv_n,
+                                             mean, stat);
+        }
+        const float rstd = rstd_from(stat, a.eps);
+        if (threadIdx.x == 0) {
+            if (a.mean_out)
+                a.mean_out[row] = mean;
+            if (a.rstd_out)
+                a.rstd_out[row] = rstd;
+        }
+        if (!EARLY)
+            load_mod();
+        const u64 mean2 = f2_splat(mean), rstd2 = f2_splat(rstd);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int v = j * 32 * WPR + threadIdx.x;
+            st_stream(out + base + v, normalise_modulate<OP>(xv[j], mean2, rstd2,
+                                                             bf2x4_add(s1[j], kBf2One), h[j],
+                                                             w[j], has_w));
+        }
+    }
+}
+
+// Launches the cooperative kernel for at most kCoopRowsPerSm rows per SM when
+// every row gets a resident CTA at once (one wave); otherwise returns false
+// and leaves the launch to the ring.  Early modulation loads measured faster
+// at 1024 and 4096 values, late ones at 3072 (where the early form needs ~127
+// registers).
+template <int OP, int V>
+bool launch_coop(const RowArgs& a, const DeviceInfo& dev, cudaStream_t stream, cudaError_t& err)
+{
+    if (a.rows > kCoopRowsPerSm * dev.sms)
+        return false;
+    auto kern = row_kernel_coop<OP, V, V != 3>;
+    static PerDeviceInt blocks_per_sm;
+    int bps = 0;
+    err = blocks_per_sm.get(dev.device, bps, [&](int& v) -> cudaError_t {
+        int n = 0;
+        const cudaError_t e =
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32 * kCoopWarps, 0);
+        v = n;
+        return e;
+    });
+    if (err != cudaSuccess)
+        return true;
+    if (a.rows > static_cast<int64_t>(bps) * dev.sms)
+        return false;
+    err = launch_dependent(kern, static_cast<int>(a.rows), 32 * kCoopWarps, 0, stream, a);
+    return true;
+}
+
 // Rows of up to 4096 values: one warp each (V vectors per lane); longer rows
 // are split over two or four warps (contiguous segments).
 template <int OP>
 cudaError_t launch_op(const RowArgs& a, const DeviceInfo& dev, cudaStream_t stream)
 {
     const int Dv = a.Dv;
+    {
+        cudaError_t e = cudaSuccess;
+        bool done = false;
+        switch (Dv) {
+        case 128:
+            done = launch_coop<OP, 1>(a, dev, stream, e);
+            break;
+        case 256:
+            done = launch_coop<OP, 2>(a, dev, stream, e);
+            break;
+        case 384:
+            done = launch_coop<OP, 3>(a, dev, stream, e);
+            break;
+        case 512:
+            done = launch_coop<OP, 4>(a, dev, stream, e);
+            break;
+        default:
+            break;
+        }
+        if (done)
+            return e;
+    }
     if (Dv <= 32)
         return launch_cfg<OP, 1, 1>(a, dev, stream);
     if (Dv <= 64)

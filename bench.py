@@ -228,6 +228,7 @@ def run_reference(args, rank, world):
 KERNEL_SOURCES = {
     "row_kernel": ("row_kernels.cu", "device_common.cuh", "launch.h"),
     "row_kernel_ws": ("row_kernels.cu", "device_common.cuh", "launch.h"),
+    "row_kernel_coop": ("row_kernels.cu", "device_common.cuh", "launch.h"),
     "qk_kernel": ("qk_kernel.cu", "device_common.cuh", "launch.h"),
     "wan_kernel": ("wan_kernel.cu", "device_common.cuh", "launch.h"),
     "bwd_ws_kernel": ("backward.cu", "device_common.cuh", "launch.h"),

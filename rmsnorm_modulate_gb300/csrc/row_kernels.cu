@@ -479,15 +479,15 @@ __global__ void __launch_bounds__(RowShape<OP, V, WPR>::kThreads, RowShape<OP, V
 // last rows set the end of the launch) 4 + 8.  4096 values: 8 + 8 warps and
 // one CTA per SM with a 176 KB ring (the epilogue's share of the work grows
 // with the weight row of RMSNorm); gated, whose slots hold two rows and
-// whose statistics warps also write the residual stream out, 4 + 12 warps
-// around 12 slots (192 KB).  At 4096 values two output warps share each row
+// whose statistics warps also write the residual stream out, 4 + 8 warps
+// around 8 slots (128 KB).  At 4096 values two output warps share each row
 // (half of its vectors each; the later of the two refills the slot), which
 // halves the epilogue latency of a CTA's last rows.
 template <int OP, int V, bool SHORT = false>
 struct WsShape {
     static constexpr bool kGatedWide = (V >= 16 && OP == kOpGated);
     static constexpr int kStatWarps = kGatedWide ? 4 : ((V < 16 && SHORT) ? 4 : 8);
-    static constexpr int kOutWarps = kGatedWide ? 12 : ((V >= 16 || SHORT) ? 8 : 4);
+    static constexpr int kOutWarps = kGatedWide ? 8 : ((V >= 16 || SHORT) ? 8 : 4);
     static constexpr int kBlocks = V >= 16 ? 1 : 2;
     static constexpr int kRingBudget = (kGatedWide ? 192 : (V >= 16 ? 176 : 100)) * 1024;
     static constexpr int kOutGroup = V >= 16 ? 2 : 1;  // output warps sharing one row
@@ -505,7 +505,7 @@ struct WsShape {
     // which take their rows in order, so no barrier is ever waited on with
     // the parity of a phase two steps ahead (which would read as complete).
     static constexpr int kSlotsRaw = kRingBudget / (kSlotVec * 16);
-    static constexpr int kSlotStep = kGatedWide ? 12 : kStatWarps;  // a multiple of both
+    static constexpr int kSlotStep = kGatedWide ? 8 : kStatWarps;  // a multiple of both
     static constexpr int kSlots = kSlotsRaw / kSlotStep * kSlotStep;
     static constexpr int kRingBytes = kSlots * kSlotVec * 16;
     static_assert(kSlots >= kStatWarps && kSlots % kStatWarps == 0 && kSlots % kOutGroups == 0,

@@ -641,7 +641,6 @@ struct BlockTrees {
 __global__ void __launch_bounds__(32 * (kBwdMaxOutWarps + kBwdStatWarps), 1)
     bwd_ws_kernel(const BwdArgs a, const int nslots)
 {
-    grid_dependency_sync();
     extern __shared__ __align__(128) uint4 smem[];
     __shared__ __align__(8) unsigned long long full_bar[kBwdMaxSlots], ready_bar[kBwdMaxSlots];
     __shared__ float4 slot_stats[kBwdMaxSlots];  // (mean, rstd, c1, c2) of the row in each slot
@@ -681,6 +680,11 @@ __global__ void __launch_bounds__(32 * (kBwdMaxOutWarps + kBwdStatWarps), 1)
             released[s] = 0;
         }
         mbar_init_fence();
+    }
+    // only shared memory so far: the barriers are ready when the previous
+    // grid's results become visible
+    grid_dependency_sync();
+    if (threadIdx.x == 0) {
         // the first nslots rows of the sequence
         SeqCursor c;
         c.start(sq, blockIdx.x);

@@ -153,7 +153,6 @@ template <int RV, int P>
 __global__ void __launch_bounds__(kWsThreads, 2)
     qk_kernel_ws(const QkArgs a, int blocks_q, FastDiv chunks_q, FastDiv chunks_k)
 {
-    grid_dependency_sync();
     using Shape = QkShape<RV, P>;
     constexpr int V = Shape::kVecPerLane;
     constexpr int kTileRows = Shape::kTileRows;
@@ -204,6 +203,9 @@ __global__ void __launch_bounds__(kWsThreads, 2)
         }
         mbar_init_fence();
     }
+    // only shared memory so far: the barriers are ready when the previous
+    // grid's results become visible
+    grid_dependency_sync();
     if (threadIdx.x < 2 * RV) {
         const uint4* __restrict__ wv = static_cast<const uint4*>(t.w);
         const uint4* __restrict__ bv = static_cast<const uint4*>(t.b);

@@ -581,7 +581,6 @@ template <int OP, int V, bool EXACT, bool SHORT>
 __global__ void __launch_bounds__(WsShape<OP, V, SHORT>::kThreads, WsShape<OP, V, SHORT>::kBlocks)
     row_kernel_ws(const RowArgs a, const Items items)
 {
-    grid_dependency_sync();
     using Shape = WsShape<OP, V, SHORT>;
     constexpr int kSlots = Shape::kSlots;
     constexpr int kSegVec = Shape::kSegVec;
@@ -626,6 +625,9 @@ __global__ void __launch_bounds__(WsShape<OP, V, SHORT>::kThreads, WsShape<OP, V
         mbar_init_fence();
     }
     __syncthreads();
+    // only shared memory so far: the barriers are ready when the previous
+    // grid's results become visible
+    grid_dependency_sync();
 
     bool broken = false;
     int64_t uses = 0;  // rows the CTA has run through its ring
